@@ -1,0 +1,432 @@
+"""Benchmark: block-skipping causal prefill attention on one 128K-token
+Llama-3-8B-shaped attention layer (Hq=32, Hkv=8, d=128, causal, bf16,
+lambda=0.01), through the library's C interface.
+
+Prints ONE JSON line. ``value`` is dense-equivalent TFLOP/s (the FLOPs of
+dense causal attention on the layer divided by the measured time), inputs
+resident in HBM; ``e2e`` is the same metric with host buffers copied in and
+the result copied out inside the timed region; ``roofline`` compares the
+forward kernel's executed tensor FLOPs (QK^T on every causal tile, P.V on
+kept tiles) with the measured dense bf16 peak; ``cpu_baseline`` times the
+fp64 CPU oracle on a bounded sample of the same layer.
+
+``--impl reference`` times the CPU oracle alone (the reference arm).
+Multi-GPU: one process per GPU (torchrun), each running the same layer
+(weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "dense-equiv TFLOP/s and ms per 128K prefill attn layer (Llama-3-8B shape)"
+TILE = 128
+WORKLOADS = {
+    "C2": "llama3-8b attention layer, 131072 tokens, Hq=32 Hkv=8 d=128, causal, bf16, lambda=0.01",
+    "C1": "llama3-8b attention layer, 32768 tokens, Hq=32 Hkv=8 d=128, causal, bf16, lambda=0.01",
+    "C3": "continuous batching, 16 sequences 4K-64K log-uniform, Hq=32 Hkv=8 d=128, causal, bf16",
+    "C0": "single head, 2048 tokens, d=128, causal, bf16",
+}
+
+
+# ------------------------------------------------------------------ work model
+
+def dense_flops(seqlens, Hq, d=128):
+    """FLOPs of dense causal attention: 2 matmuls x 2 flop x d x L(L+1)/2 per head."""
+    return sum(Hq * 4.0 * d * L * (L + 1) / 2.0 for L in seqlens)
+
+
+def causal_tiles(seqlens, Hq):
+    return sum(Hq * n * (n + 1) // 2 for n in ((L + TILE - 1) // TILE for L in seqlens))
+
+
+def executed_flops(seqlens, Hq, skipped_tiles, d=128):
+    """Tensor FLOPs the kernel issues: QK^T on every causal tile, P.V on kept ones."""
+    per_tile = 2.0 * TILE * TILE * d
+    ct = causal_tiles(seqlens, Hq)
+    return per_tile * (ct + (ct - skipped_tiles))
+
+
+def popcount(words: np.ndarray) -> int:
+    return int(np.unpackbits(np.ascontiguousarray(words).view(np.uint8)).sum())
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def _oracle_item(args):
+    """Worker: run the oracle's tile walk on one query tile of the saved layer."""
+    path, Hq, Hkv, item = args
+    import numpy as np  # noqa: F811
+    from oracle import numerics, tile_walk
+    q = np.load(os.path.join(path, "q.npy"), mmap_mode="r")
+    k = np.load(os.path.join(path, "k.npy"), mmap_mode="r")
+    v = np.load(os.path.join(path, "v.npy"), mmap_mode="r")
+    s, h, i = item
+    g = h // (Hq // Hkv)
+    hi = (i + 1) * TILE                       # keys past the diagonal tile are never visited
+    qs = numerics.bf16_to_f64(q[:hi, h:h + 1])
+    ks = numerics.bf16_to_f64(k[:hi, g:g + 1])
+    vs = numerics.bf16_to_f64(v[:hi, g:g + 1])
+    t0 = time.perf_counter()
+    tile_walk.walk_one(qs, ks, vs, [0, hi], 1, 1, True, 0.01, 1.0 / math.sqrt(128), (0, 0, i))
+    return time.perf_counter() - t0
+
+
+def item_dense_flops(i, d=128):
+    rows = np.arange(i * TILE, (i + 1) * TILE) + 1
+    return 4.0 * d * float(rows.sum())
+
+
+def oracle_baseline(problem, budget_s: float = 12.0, cores=None, seed: int = 0):
+    """Time the oracle on a bounded, deterministic sample of query tiles.
+
+    Returns (dense-equivalent TFLOP/s over the sample, cores, description).
+    """
+    import multiprocessing as mp
+    cores = cores or len(os.sched_getaffinity(0))
+    tmp = tempfile.mkdtemp(prefix="bsa_oracle_")
+    np.save(os.path.join(tmp, "q.npy"), problem.q)
+    np.save(os.path.join(tmp, "k.npy"), problem.k)
+    np.save(os.path.join(tmp, "v.npy"), problem.v)
+    n = (int(problem.seqlens[0]) + TILE - 1) // TILE
+    rng = np.random.default_rng(seed)
+    env_keep = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in env_keep:
+        os.environ[k] = "1"
+    ctx = mp.get_context("spawn")
+    try:
+        with ctx.Pool(cores) as pool:
+            # calibrate on one mid-length tile per worker
+            cal = [(tmp, problem.Hq, problem.Hkv, (0, int(rng.integers(problem.Hq)), n // 2))
+                   for _ in range(cores)]
+            t_cal = statistics.median(pool.map(_oracle_item, cal))
+            per_visit = t_cal / (n // 2 + 1)
+            visits = max(cores, int(budget_s * cores / per_visit))
+            items, total = [], 0
+            while total < visits:
+                i = int(rng.integers(n))
+                items.append((tmp, problem.Hq, problem.Hkv, (0, int(rng.integers(problem.Hq)), i)))
+                total += i + 1
+            t0 = time.perf_counter()
+            pool.map(_oracle_item, items, chunksize=1)
+            wall = time.perf_counter() - t0
+    finally:
+        for k, val in env_keep.items():
+            if val is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = val
+        for f in ("q.npy", "k.npy", "v.npy"):
+            os.unlink(os.path.join(tmp, f))
+        os.rmdir(tmp)
+    flops = sum(item_dense_flops(it[3][2]) for it in items)
+    desc = (f"{len(items)} random query tiles (all key tiles up to the diagonal) of the layer, "
+            f"{total} tile visits, {cores} worker processes x 1 thread, fp64")
+    return flops / wall / 1e12, cores, desc, wall, len(items)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+
+    from dynamic_block_sparse_causal_gb300 import bsa
+    from gen import inputs as gi
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    bsa.lib()
+    p = gi.config(args.config, seed=args.seed, lam=args.lam)
+    seqlens = [int(x) for x in p.seqlens]
+    T, Hq, Hkv, d = p.total_tokens, p.Hq, p.Hkv, p.d
+    dflops = dense_flops(seqlens, Hq, d)
+    stream = torch.cuda.current_stream()
+
+    def upload(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q, k, v = upload(p.q), upload(p.k), upload(p.v)
+    cu = torch.from_numpy(p.cu_seqlens).to(dev)
+    out = torch.empty((T, Hq, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
+    nw = bsa.skip_bitmap_words(p.cu_seqlens, Hq)
+    bm = torch.empty((nw,), dtype=torch.int32, device=dev)
+
+    def step(lam=args.lam):
+        st = bsa.prefill_fwd(q, k, v, cu, p.n_seqs, Hq, Hkv, d, 1, lam, bsa.BSA_BF16, out, lse, bm, stream)
+        if st != 0:
+            raise bsa.BsaError(st, "bsa_prefill_fwd")
+
+    def timed(nsteps, lam=args.lam):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(nsteps):
+            step(lam)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return ev0.elapsed_time(ev1) / nsteps
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    bsa.check(bsa.get_device_status(stream), "device status")
+    with ClockSampler(local_rank) as clk:
+        ms = timed(args.steps)
+    clocks = clk.summary()
+    ms = max_over_ranks(ms, world, dev)
+    bsa.check(bsa.get_device_status(stream), "device status")
+    skipped = popcount(bm.cpu().numpy())
+    ctiles = causal_tiles(seqlens, Hq)
+    xflops = executed_flops(seqlens, Hq, skipped, d)
+    value = dflops * world / (ms * 1e-3) / 1e12
+
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    peak = peaks.get("bf16_tflops", 1900.0)
+    achieved = xflops / (ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_source": "MEASURED_PEAKS.json bf16_tflops (burst)" if "bf16_tflops" in peaks
+                else "fallback 1900 TFLOP/s", "flops_per_launch": xflops}
+
+    # lambda sweep on the same layer (skip fraction and TFLOP/s for each lambda)
+    sweep = []
+    if not args.no_sweep:
+        for lam in (0.0, 1e-3, 1e-2, 5e-2):
+            step(lam)
+            torch.cuda.synchronize()
+            m = timed(max(2, args.steps // 2), lam)
+            sk = popcount(bm.cpu().numpy())
+            sweep.append({"lambda": lam, "ms": round(m, 3), "dense_equiv_tflops": round(dflops / m / 1e9, 1),
+                          "executed_tflops": round(executed_flops(seqlens, Hq, sk, d) / m / 1e9, 1),
+                          "skip_fraction": round(sk / ctiles, 5)})
+
+    # end to end through the C interface with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq = torch.from_numpy(p.q.view(np.int16)).pin_memory()
+        hk = torch.from_numpy(p.k.view(np.int16)).pin_memory()
+        hv = torch.from_numpy(p.v.view(np.int16)).pin_memory()
+        hcu = torch.from_numpy(p.cu_seqlens).pin_memory()
+        hout = torch.empty((T, Hq, d), dtype=torch.int16).pin_memory()
+        hlse = torch.empty((Hq, T), dtype=torch.float32).pin_memory()
+        hbm = torch.empty((nw,), dtype=torch.int32).pin_memory()
+
+        def e2e_step():
+            q.view(torch.int16).copy_(hq, non_blocking=True)
+            k.view(torch.int16).copy_(hk, non_blocking=True)
+            v.view(torch.int16).copy_(hv, non_blocking=True)
+            cu.copy_(hcu, non_blocking=True)
+            step()
+            hout.copy_(out.view(torch.int16), non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+            hbm.copy_(bm, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(2, args.steps // 2)
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        ms_e2e = max_over_ranks((time.perf_counter() - t0) * 1e3 / n_e2e, world, dev)
+        h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + hcu.numel() * 4
+        d2h = hout.numel() * 2 + hlse.numel() * 4 + hbm.numel() * 4
+        e2e = {"value": round(dflops * world / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "ms_per_step": round(ms_e2e, 3), "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+        bsa.check(bsa.get_device_status(stream), "device status")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, cores, desc, wall, nitems = oracle_baseline(p, budget_s=args.cpu_budget)
+        cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
+               "wall_s": round(wall, 2)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded generator: sink + local-window bias, Llama-3-8B attention shape)",
+        "config": {"workload": WORKLOADS.get(args.config, args.config), "name": args.config,
+                   "tokens": T, "Hq": Hq, "Hkv": Hkv, "d": d, "lambda": args.lam, "causal": True,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (q/out 1.07 GB each, k/v 0.27 GB each); no flush"},
+        "skip_fraction": round(skipped / ctiles, 5), "executed_tflop_per_step": round(xflops / 1e12, 3),
+        "dense_equiv_tflop_per_step": round(dflops / 1e12, 3),
+        "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
+        "gpu_launches": 2 * args.steps, "lambda_sweep": sweep,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def reference_arm(args, rank, world):
+    """The CPU oracle, as it stands, on a bounded sample of the same layer."""
+    if rank != 0:
+        return
+    from gen import inputs as gi
+    p = gi.config(args.config, seed=args.seed, lam=args.lam)
+    vals = []
+    for _ in range(args.warmup):
+        oracle_baseline(p, budget_s=2.0)
+    for _ in range(args.steps):
+        tf, cores, desc, wall, nitems = oracle_baseline(p, budget_s=args.ref_budget)
+        vals.append((tf, wall))
+    tf = statistics.median(v[0] for v in vals)
+    dflops = dense_flops([int(x) for x in p.seqlens], p.Hq, p.d)
+    ms = dflops / (tf * 1e12) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(tf, 6), "unit": "TFLOP/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generator)",
+        "config": {"workload": WORKLOADS.get(args.config, args.config), "name": args.config,
+                   "lambda": args.lam, "causal": True},
+        "cpu_baseline": {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": desc + "; ms_per_step extrapolated to the whole layer"},
+        "e2e": {"value": round(tf, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--config", default="C2", choices=sorted(WORKLOADS))
+    ap.add_argument("--lam", type=float, default=0.01)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds per reference step")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "gpu":
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+    else:
+        gpu_arm(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

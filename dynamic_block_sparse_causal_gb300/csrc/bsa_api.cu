@@ -1,0 +1,268 @@
+// C interface of libbsa (declared in include/bsa.h): argument checks,
+// per-stream scratch areas, TMA tensor-map templates, launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "bsa.h"
+#include "bsa_internal.h"
+
+namespace {
+
+using bsa::Workspace;
+using bsa::WorkspaceLayout;
+
+struct StreamScratch {
+  Workspace *ws = nullptr;
+  size_t bytes = 0;
+};
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  int sm_count = 0;
+};
+
+std::mutex g_mu;
+std::map<std::pair<int, cudaStream_t>, StreamScratch> g_scratch;
+std::map<int, DeviceInfo> g_devices;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+thread_local const float *t_q_scale = nullptr;
+thread_local const float *t_k_scale = nullptr;
+thread_local const float *t_v_scale = nullptr;
+thread_local int32_t t_drop_k_load = -1;
+thread_local uint64_t t_wait_limit_ns = 2000000000ull;  // 2 s
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Resolve the driver's tensor-map encoder once (no link-time libcuda).
+bool encoder() {
+  if (g_encode) return true;
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+bsa_status_t device_info(int dev, DeviceInfo **out) {
+  DeviceInfo &d = g_devices[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return BSA_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);
+    if (d.supported && bsa::prepare_forward() != cudaSuccess) return BSA_ERR_CUDA;
+    d.ready = true;
+  }
+  *out = &d;
+  return BSA_OK;
+}
+
+// Scratch area of (device, stream), grown stream-ordered when n_seqs grows.
+bsa_status_t scratch_for(int dev, cudaStream_t stream, size_t bytes, Workspace **out) {
+  StreamScratch &s = g_scratch[{dev, stream}];
+  if (s.bytes < bytes) {
+    void *p = nullptr;
+    if (cudaMallocAsync(&p, bytes, stream) != cudaSuccess) return BSA_ERR_NO_MEMORY;
+    if (cudaMemsetAsync(p, 0, sizeof(Workspace), stream) != cudaSuccess) return BSA_ERR_CUDA;
+    if (s.ws) {  // keep the sticky status word
+      if (cudaMemcpyAsync(&static_cast<Workspace *>(p)->status, &s.ws->status, sizeof(int32_t),
+                          cudaMemcpyDeviceToDevice, stream) != cudaSuccess ||
+          cudaFreeAsync(s.ws, stream) != cudaSuccess)
+        return BSA_ERR_CUDA;
+    }
+    s.ws = static_cast<Workspace *>(p);
+    s.bytes = bytes;
+  }
+  *out = s.ws;
+  return BSA_OK;
+}
+
+// [tokens, H, 128] tiles of 128 rows x 128 bytes, 128-byte swizzle. The token
+// extent is a placeholder (1) that the prologue replaces with cu[n_seqs].
+bool encode_tile_map(CUtensorMap *m, const void *base, int H, bool fp8) {
+  const cuuint64_t elem = fp8 ? 1 : 2;
+  cuuint64_t dims[3] = {(cuuint64_t)bsa::kHeadDim, (cuuint64_t)H, 1};
+  cuuint64_t strides[2] = {bsa::kHeadDim * elem, (cuuint64_t)H * bsa::kHeadDim * elem};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / elem), 1, (cuuint32_t)bsa::kTile};
+  cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult r =
+      g_encode(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+               const_cast<void *>(base), dims, strides, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+bsa_status_t bsa_prefill_fwd(const void *q, const void *k, const void *v,
+                             const int32_t *cu_seqlens, int32_t n_seqs, int32_t Hq, int32_t Hkv,
+                             int32_t d, int32_t causal, float lambda, bsa_dtype_t dtype,
+                             void *out, float *lse, uint32_t *skip_bitmap,
+                             bsa_stream_t stream_) {
+  // ---- host-only checks: nothing is enqueued on failure
+  if (!q || !k || !v || !cu_seqlens || !out) return BSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(cu_seqlens, 4) || !aligned(lse, 4) || !aligned(skip_bitmap, 4))
+    return BSA_ERR_INVALID_ARG;
+  if (n_seqs < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Hq > 65535) return BSA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return BSA_ERR_INVALID_ARG;
+  if (!(lambda >= 0.0f && lambda < 1.0f)) return BSA_ERR_INVALID_ARG;  // also rejects NaN
+  if (dtype != BSA_BF16 && dtype != BSA_FP8_E4M3) return BSA_ERR_INVALID_ARG;
+  const bool fp8 = dtype == BSA_FP8_E4M3;
+  if (fp8 && (!t_q_scale || !t_k_scale || !t_v_scale)) return BSA_ERR_INVALID_ARG;
+  if (d != bsa::kHeadDim) return BSA_ERR_UNSUPPORTED;
+
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo *info = nullptr;
+  bsa_status_t st = device_info(dev, &info);
+  if (st != BSA_OK) return st;
+  if (!info->supported) return BSA_ERR_UNSUPPORTED;
+  if (!encoder()) return BSA_ERR_CUDA;
+
+  CUtensorMap tmpl[3];
+  if (!encode_tile_map(&tmpl[0], q, Hq, fp8) || !encode_tile_map(&tmpl[1], k, Hkv, fp8) ||
+      !encode_tile_map(&tmpl[2], v, Hkv, fp8))
+    return BSA_ERR_INVALID_ARG;
+
+  const WorkspaceLayout layout = WorkspaceLayout::make(n_seqs);
+  Workspace *ws = nullptr;
+  if ((st = scratch_for(dev, stream, layout.bytes, &ws)) != BSA_OK) return st;
+  if (bsa::launch_prologue(cu_seqlens, n_seqs, Hq, Hkv, ws, layout, tmpl, stream) != cudaSuccess)
+    return BSA_ERR_CUDA;
+
+  char *base = reinterpret_cast<char *>(ws);
+  bsa::FwdParams p{};
+  p.ws = ws;
+  p.seq_sorted = reinterpret_cast<const int32_t *>(base + layout.seq_sorted);
+  p.seq_bitmap_off = reinterpret_cast<const int64_t *>(base + layout.seq_bitmap_off);
+  p.level_start = reinterpret_cast<const int32_t *>(base + layout.level_start);
+  p.cu_seqlens = cu_seqlens;
+  p.out = out;
+  p.lse = lse;
+  p.bitmap = skip_bitmap;
+  p.q_scale = fp8 ? t_q_scale : nullptr;
+  p.k_scale = fp8 ? t_k_scale : nullptr;
+  p.v_scale = fp8 ? t_v_scale : nullptr;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.group = Hq / Hkv;
+  p.pairs_per_group = (p.group + 1) / 2;
+  p.causal = causal;
+  p.c = (float)(1.0 / std::sqrt((double)d) * 1.4426950408889634);
+  p.log2_lambda = lambda > 0.f ? (float)std::log2((double)lambda) : -INFINITY;
+  p.wait_limit_ns = t_wait_limit_ns;
+  p.debug_drop_k_load = t_drop_k_load;
+  if (bsa::launch_forward(p, fp8, info->sm_count, stream) != cudaSuccess) return BSA_ERR_CUDA;
+  return BSA_OK;
+}
+
+bsa_status_t bsa_set_fp8_scales(const float *q_scale, const float *k_scale,
+                                const float *v_scale) {
+  const int nulls = !q_scale + !k_scale + !v_scale;
+  if (nulls != 0 && nulls != 3) return BSA_ERR_INVALID_ARG;
+  if (!aligned(q_scale, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
+    return BSA_ERR_INVALID_ARG;
+  t_q_scale = q_scale;
+  t_k_scale = k_scale;
+  t_v_scale = v_scale;
+  return BSA_OK;
+}
+
+bsa_status_t bsa_quantize_fp8(const void *x_bf16, int64_t tokens, int32_t H, int32_t d,
+                              uint8_t *x_e4m3, float *scale, bsa_stream_t stream) {
+  if (!x_bf16 || !x_e4m3 || !scale) return BSA_ERR_INVALID_ARG;
+  if (!aligned(x_bf16, 16) || !aligned(x_e4m3, 8) || !aligned(scale, 4)) return BSA_ERR_INVALID_ARG;
+  if (tokens < 0 || H < 1 || H > 1024 || d < 8 || d % 8 != 0) return BSA_ERR_INVALID_ARG;
+  if (bsa::launch_quantize_fp8(x_bf16, tokens, H, d, x_e4m3, scale,
+                               reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  return BSA_OK;
+}
+
+int64_t bsa_skip_bitmap_words(const int32_t *cu, int32_t n_seqs, int32_t Hq) {
+  if (!cu || n_seqs < 1 || Hq < 1 || cu[0] != 0) return -1;
+  int64_t words = 0;
+  for (int32_t s = 0; s < n_seqs; ++s) {
+    const int64_t L = (int64_t)cu[s + 1] - cu[s];
+    if (L < 0) return -1;
+    const int64_t n = (L + bsa::kTile - 1) / bsa::kTile;
+    words += (int64_t)Hq * n * ((n + 31) / 32);
+  }
+  return words;
+}
+
+bsa_status_t bsa_get_device_status(bsa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return BSA_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto it = g_scratch.find({dev, stream});
+  if (it == g_scratch.end() || !it->second.ws) return BSA_OK;
+  int32_t status = 0;
+  if (cudaMemcpy(&status, &it->second.ws->status, sizeof(status), cudaMemcpyDeviceToHost) !=
+          cudaSuccess ||
+      cudaMemset(&it->second.ws->status, 0, sizeof(status)) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  if (status & bsa::kStatusBadSeqlens) return BSA_ERR_BAD_SEQLENS;
+  if (status & bsa::kStatusTimeout) return BSA_ERR_TIMEOUT;
+  return BSA_OK;
+}
+
+const char *bsa_status_string(bsa_status_t s) {
+  switch (s) {
+    case BSA_OK: return "ok";
+    case BSA_ERR_INVALID_ARG: return "invalid argument";
+    case BSA_ERR_UNSUPPORTED: return "unsupported device or head dimension";
+    case BSA_ERR_CUDA: return "CUDA error";
+    case BSA_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case BSA_ERR_NO_MEMORY: return "scratch allocation failed";
+    case BSA_ERR_BAD_SEQLENS: return "cu_seqlens is not a valid prefix sum";
+  }
+  return "unknown status";
+}
+
+int32_t bsa_version(void) { return 100; }
+
+void bsa_release(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (auto &kv : g_scratch) {
+    if (kv.second.ws) {
+      cudaSetDevice(kv.first.first);
+      cudaFree(kv.second.ws);
+    }
+  }
+  g_scratch.clear();
+  cudaSetDevice(cur);
+}
+
+bsa_status_t bsa_debug_fault_drill(int32_t drop_k_load, int64_t wait_limit_ns) {
+  if (wait_limit_ns <= 0 || drop_k_load < -1) return BSA_ERR_INVALID_ARG;
+  t_drop_k_load = drop_k_load;
+  t_wait_limit_ns = (uint64_t)wait_limit_ns;
+  return BSA_OK;
+}
+
+}  // extern "C"

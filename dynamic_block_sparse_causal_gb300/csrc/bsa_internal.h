@@ -1,0 +1,83 @@
+// Internal structures shared by the host interface and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace bsa {
+
+constexpr int kTile = 128;          // query / key tile edge (block_size)
+constexpr int kHeadDim = 128;       // the only supported head dimension
+constexpr int kMaxLevels = 65536;   // longest sequence: 65536 tiles = 8M tokens
+constexpr int kFwdThreads = 384;    // 4 control warps + 2 softmax warpgroups
+
+// Bits of the device status word.
+constexpr int kStatusBadSeqlens = 1 << 0;
+constexpr int kStatusTimeout = 1 << 1;
+
+// Per-stream scratch area, written by the prologue kernel and read by the
+// forward kernel. Variable-length tables follow the header:
+//   int32 seq_sorted[n_seqs]      sequences by tile count, longest first
+//   int64 seq_bitmap_off[n_seqs]  first skip-bitmap word of each sequence
+//   int32 level_start[kMaxLevels] first work item of each query-tile level
+struct alignas(128) Workspace {
+  CUtensorMap tmap[3];   // q, k, v tile maps; token extent patched on device
+  int32_t counter;       // next work item (atomic)
+  int32_t status;        // kStatus* bits, sticky until read by the host
+  int32_t total_items;   // 0 when cu_seqlens was rejected
+  int32_t max_tiles;     // longest sequence, in tiles
+  int32_t total_tokens;  // cu_seqlens[n_seqs]
+  int32_t pad_[27];
+};
+
+struct WorkspaceLayout {
+  size_t seq_sorted, seq_bitmap_off, level_start, bytes;
+  static WorkspaceLayout make(int n_seqs) {
+    WorkspaceLayout l;
+    size_t off = sizeof(Workspace);
+    l.seq_sorted = off;
+    off += ((size_t)n_seqs * 4 + 127) / 128 * 128;
+    l.seq_bitmap_off = off;
+    off += ((size_t)n_seqs * 8 + 127) / 128 * 128;
+    l.level_start = off;
+    off += (size_t)kMaxLevels * 4;
+    l.bytes = off;
+    return l;
+  }
+};
+
+struct FwdParams {
+  Workspace *ws;
+  const int32_t *seq_sorted;
+  const int64_t *seq_bitmap_off;
+  const int32_t *level_start;
+  const int32_t *cu_seqlens;
+  void *out;                 // bf16 [T, Hq, d]
+  float *lse;                // [Hq, T] or null
+  uint32_t *bitmap;          // or null
+  const float *q_scale;      // fp8 only
+  const float *k_scale;
+  const float *v_scale;
+  int32_t Hq, Hkv, group;    // group = Hq / Hkv
+  int32_t pairs_per_group;   // ceil(group / 2): query heads are handled two at a time
+  int32_t causal;
+  float c;                   // softmax scale * log2(e)
+  float log2_lambda;         // -inf when skipping is off
+  uint64_t wait_limit_ns;    // bound on every pipeline wait
+  int32_t debug_drop_k_load; // >= 0: the producer omits that K load (fault drill)
+};
+
+// Host-side launchers (bsa_fwd.cu).
+cudaError_t launch_prologue(const int32_t *cu_seqlens, int n_seqs, int Hq, int Hkv,
+                            Workspace *ws, const WorkspaceLayout &layout,
+                            const CUtensorMap tmpl[3], cudaStream_t stream);
+cudaError_t launch_forward(const FwdParams &p, bool fp8, int num_ctas, cudaStream_t stream);
+size_t forward_smem_bytes();
+cudaError_t prepare_forward();   // per device: opt in to the shared-memory size
+
+// FP8 quantiser (bsa_quant.cu).
+cudaError_t launch_quantize_fp8(const void *x, int64_t tokens, int H, int d, uint8_t *codes,
+                                float *scale, cudaStream_t stream);
+
+}  // namespace bsa

@@ -1,0 +1,172 @@
+/*
+ * bsa.h -- C interface of the GB300 (sm_103a) block-skipping causal prefill
+ * attention library (libbsa.so).
+ *
+ * The operation is the one of the dynamic sparse attention deployment guide
+ * ("长上下文推理加速方案部署实战：基于动态稀疏注意力机制的推理服务优化指南",
+ * cloud.baidu.com article 9427124), §3.2 "dynamic sparse attention kernel":
+ * a flash-style forward pass over 128x128 query/key tiles with an online
+ * softmax. Key tiles are visited in ascending order; for each one the
+ * per-row tile maximum of the scores is compared with the running row
+ * maximum, and the tile is skipped -- no exponentials, no V load, no P.V
+ * product -- when for every valid row of the query tile
+ *
+ *        tile_max(row) < running_max(row) + ln(lambda).
+ *
+ * §3.3 / §6.1 fix the direction (a larger lambda prunes more blocks) and
+ * §5 step 3 the defaults (lambda = 0.01, block 128); lambda = 0 turns the
+ * rule off and gives exact dense causal attention. GQA support is required
+ * by §5 step 4; packed variable-length batches (continuous batching) and FP8
+ * are the capabilities the block-sparse prefill monitoring page lists for
+ * production prefill kernels.
+ *
+ * Conventions for every entry point:
+ *  - All pointers named "device" must point to memory of the current CUDA
+ *    device. The caller owns every buffer; the library never frees them and
+ *    never writes to inputs.
+ *  - Work is enqueued on `stream` (NULL = legacy default stream) and is fully
+ *    asynchronous: no host synchronisation, no host read of device data.
+ *  - Arguments are validated on the host before anything is launched; an
+ *    invalid call returns its status and enqueues nothing. Launch failures
+ *    return BSA_ERR_CUDA. Errors found on the device (malformed cu_seqlens, a
+ *    pipeline wait that ran out) are recorded in a per-stream status word
+ *    that bsa_get_device_status() reads.
+ *  - Calls on distinct streams may run concurrently; each stream has its own
+ *    library-owned scratch area (work queue, tensor maps), grown on demand.
+ */
+#ifndef BSA_H
+#define BSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so the header needs no CUDA. */
+typedef struct CUstream_st *bsa_stream_t;
+
+typedef enum {
+  BSA_BF16 = 0,     /* q, k, v are bfloat16 */
+  BSA_FP8_E4M3 = 1  /* q, k, v are FP8 E4M3 codes with per-head scales */
+} bsa_dtype_t;
+
+typedef enum {
+  BSA_OK = 0,
+  BSA_ERR_INVALID_ARG = 1,  /* a host-checkable argument is out of range   */
+  BSA_ERR_UNSUPPORTED = 2,  /* device is not sm_103, or d != 128           */
+  BSA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed        */
+  BSA_ERR_TIMEOUT = 4,      /* a device-side pipeline wait ran out         */
+  BSA_ERR_NO_MEMORY = 5,    /* scratch allocation failed                   */
+  BSA_ERR_BAD_SEQLENS = 6   /* device cu_seqlens not a valid prefix sum    */
+} bsa_status_t;
+
+/*
+ * Block-skipping causal prefill attention, forward.
+ *
+ * q            device, [total_tokens, Hq, d] row-major (d fastest), 16-byte
+ *              aligned; element type from `dtype`.
+ * k, v         device, [total_tokens, Hkv, d], same type and alignment.
+ * cu_seqlens   device int32 [n_seqs + 1]: cu[0] = 0, non-decreasing,
+ *              cu[n_seqs] = total_tokens. Sequence s is rows
+ *              cu[s] .. cu[s+1]-1 of q/k/v/out. total_tokens must not exceed
+ *              the rows allocated in q, k, v and out (the library cannot
+ *              check this). Validated on the device: a violation writes
+ *              nothing, and records BSA_ERR_BAD_SEQLENS.
+ * n_seqs       >= 1. Hq, Hkv >= 1 with Hq % Hkv == 0; query head h reads
+ *              key/value head h / (Hq / Hkv) (grouped-query attention).
+ * d            head dimension; 128 is the only supported value.
+ * causal       1: causal (key position <= query position); 0: every key of
+ *              the sequence is visible (same skip rule, all tiles visited).
+ * lambda       skip threshold, 0 <= lambda < 1; 0 disables skipping. NaN
+ *              is rejected.
+ * dtype        BSA_BF16, or BSA_FP8_E4M3 with scales set by
+ *              bsa_set_fp8_scales() on the calling thread.
+ * out          device bfloat16 [total_tokens, Hq, d]; must not overlap the
+ *              inputs. Every row of every sequence is written.
+ * lse          device float32 [Hq, total_tokens] or NULL: natural-log
+ *              log-sum-exp of the scaled scores over the kept entries.
+ * skip_bitmap  device uint32 or NULL. For sequence s with n_s =
+ *              ceil(L_s/128) tiles and W_s = ceil(n_s/32) words per row,
+ *              row (s, h, i) starts at word sum_{t<s}(Hq n_t W_t) +
+ *              (h n_s + i) W_s; bit j%32 of word j/32 is 1 when key tile j
+ *              was skipped for query tile i. Unvisited tiles read 0. Size
+ *              in words: bsa_skip_bitmap_words().
+ * stream       CUDA stream.
+ *
+ * The softmax scale is 1/sqrt(d). Scores are accumulated in fp32 on the
+ * tensor cores; exponentials are base-2 on the scaled scores.
+ */
+bsa_status_t bsa_prefill_fwd(const void *q, const void *k, const void *v,
+                             const int32_t *cu_seqlens, int32_t n_seqs,
+                             int32_t Hq, int32_t Hkv, int32_t d, int32_t causal,
+                             float lambda, bsa_dtype_t dtype, void *out,
+                             float *lse, uint32_t *skip_bitmap,
+                             bsa_stream_t stream);
+
+/*
+ * Per-head dequantisation scales for the next BSA_FP8_E4M3 calls made on this
+ * host thread: device float32 arrays q_scale [Hq], k_scale [Hkv],
+ * v_scale [Hkv]; a stored code x8 stands for x8 * scale. The pointers are
+ * kept (not copied) and must stay valid while such calls run. Passing three
+ * NULLs clears them. Returns BSA_ERR_INVALID_ARG if only some are NULL.
+ */
+bsa_status_t bsa_set_fp8_scales(const float *q_scale, const float *k_scale,
+                                const float *v_scale);
+
+/*
+ * Per-head FP8 E4M3 quantisation of a bfloat16 tensor x [tokens, H, d]
+ * (device, 16-byte aligned): scale[h] = max|x[:, h, :]| / 448 in float32
+ * (1.0 for an all-zero head), codes = E4M3(x / scale) rounded to nearest
+ * even with saturation to +-448. x_e4m3 device uint8 [tokens, H, d];
+ * scale device float32 [H]. d must be a multiple of 8; tokens >= 0.
+ */
+bsa_status_t bsa_quantize_fp8(const void *x_bf16, int64_t tokens, int32_t H,
+                              int32_t d, uint8_t *x_e4m3, float *scale,
+                              bsa_stream_t stream);
+
+/*
+ * Number of uint32 words of the skip bitmap for a batch, from a HOST copy of
+ * cu_seqlens. Returns -1 for a malformed cu_seqlens or n_seqs < 1, Hq < 1.
+ */
+int64_t bsa_skip_bitmap_words(const int32_t *cu_seqlens_host, int32_t n_seqs,
+                              int32_t Hq);
+
+/*
+ * Synchronises `stream`, returns the device-side status recorded by the
+ * calls made on it since the last read (BSA_OK, BSA_ERR_BAD_SEQLENS or
+ * BSA_ERR_TIMEOUT) and clears it. BSA_ERR_CUDA if the synchronisation
+ * itself fails.
+ */
+bsa_status_t bsa_get_device_status(bsa_stream_t stream);
+
+/*
+ * Fault drill, for tests of the failure path only. For the calling host
+ * thread, later bsa_prefill_fwd calls bound every device pipeline wait by
+ * wait_limit_ns, and, when drop_k_load >= 0, the TMA producer of every CTA
+ * leaves out its drop_k_load-th K tile load so that the MMA warp's wait for
+ * it runs out. The kernel then records BSA_ERR_TIMEOUT (read it with
+ * bsa_get_device_status), waits with the same bound for the copies and MMAs
+ * it has in flight, frees its tensor memory and returns; the context stays
+ * usable. bsa_debug_fault_drill(-1, 2000000000) restores the defaults.
+ */
+bsa_status_t bsa_debug_fault_drill(int32_t drop_k_load, int64_t wait_limit_ns);
+
+/* Static text for a status code. */
+const char *bsa_status_string(bsa_status_t status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t bsa_version(void);
+
+/*
+ * Frees all cached scratch areas. Must not be called while work issued by
+ * this library is still running on any stream.
+ */
+void bsa_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSA_H */
