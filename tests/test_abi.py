@@ -1,0 +1,127 @@
+"""The C interface without a GPU: the library loads, exports every entry
+point include/bsa.h declares, and rejects invalid arguments before touching
+CUDA. Also the host-side bitmap-size helper against the layout restated in
+the oracle, and the multi-process max-over-ranks reduction of bench.py on
+two gloo ranks.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import layout
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from dynamic_block_sparse_causal_gb300 import build, bsa
+    if not os.path.exists(build.LIB_PATH):
+        build.build()
+    return bsa
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "bsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    lib = L.lib()
+    names = declared_functions()
+    assert "bsa_prefill_fwd" in names and len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(L):
+    assert L.status_string(0) == "ok"
+    assert "timed out" in L.status_string(4)
+    assert L.version() >= 100
+
+
+def call(L, **over):
+    a = dict(q=16, k=32, v=48, cu=64, n_seqs=1, Hq=4, Hkv=2, d=128, causal=1, lam=0.01, dtype=0,
+             out=80, lse=None, bm=None)
+    a.update(over)
+    return L.prefill_fwd(a["q"], a["k"], a["v"], a["cu"], a["n_seqs"], a["Hq"], a["Hkv"], a["d"],
+                         a["causal"], a["lam"], a["dtype"], a["out"], a["lse"], a["bm"])
+
+
+@pytest.mark.parametrize("over,want", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(cu=None), 1), (dict(out=None), 1),
+    (dict(q=18), 1), (dict(out=8), 1), (dict(cu=66), 1), (dict(lse=2), 1), (dict(bm=6), 1),
+    (dict(n_seqs=0), 1), (dict(Hq=0), 1), (dict(Hkv=0), 1), (dict(Hq=6, Hkv=4), 1),
+    (dict(causal=2), 1), (dict(lam=-0.1), 1), (dict(lam=1.0), 1), (dict(lam=math.nan), 1),
+    (dict(lam=math.inf), 1), (dict(dtype=7), 1), (dict(dtype=1), 1),   # fp8 without scales
+    (dict(d=64), 2), (dict(d=256), 2),
+])
+def test_invalid_arguments_rejected_before_cuda(L, over, want):
+    assert call(L, **over) == want
+
+
+def test_fp8_scales_all_or_nothing(L):
+    assert L.set_fp8_scales(16, None, None) == 1
+    assert L.set_fp8_scales(None, None, None) == 0
+
+
+def test_quantize_argument_checks(L):
+    assert L.quantize_fp8(None, 10, 2, 128, 16, 16) == 1
+    assert L.quantize_fp8(16, -1, 2, 128, 16, 16) == 1
+    assert L.quantize_fp8(16, 10, 2, 12, 16, 16) == 1
+    assert L.quantize_fp8(18, 10, 2, 128, 16, 16) == 1
+
+
+def test_fault_drill_argument_checks(L):
+    assert L.debug_fault_drill(-2, 10) == 1
+    assert L.debug_fault_drill(-1, 0) == 1
+    assert L.debug_fault_drill(-1, 2000000000) == 0
+
+
+@pytest.mark.parametrize("cu,Hq", [([0, 2048], 1), ([0, 300, 5000], 2), ([0, 131072], 32),
+                                   ([0, 1, 78, 206], 2), ([0, 0, 129, 129], 3)])
+def test_bitmap_words_match_layout(L, cu, Hq):
+    assert L.skip_bitmap_words(np.array(cu, np.int32), Hq) == layout.total_words(cu, Hq)
+
+
+def test_bitmap_words_rejects_bad_seqlens(L):
+    assert L.skip_bitmap_words(np.array([1, 5], np.int32), 1) == -1
+    assert L.skip_bitmap_words(np.array([0, 5, 3], np.int32), 1) == -1
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    t = bench.max_over_ranks(10.0 + rank, world)
+    bench.barrier(world)
+    q.put((rank, t))
+    dist.destroy_process_group()
+
+
+def test_bench_max_over_ranks_gloo():
+    import multiprocessing as mp
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+    got = sorted(q.get(timeout=5) for _ in range(2))
+    assert got == [(0, 11.0), (1, 11.0)]

@@ -8,6 +8,7 @@ from __future__ import annotations
 
 import numpy as np
 import pytest
+import torch
 
 import _cases
 import _gpu
@@ -19,8 +20,9 @@ pytestmark = pytest.mark.gpu
 def test_c0(lam):
     p = _cases.small_problem("C0")
     g = _gpu.run(p, lam=lam)
-    assert np.isfinite(g["out"]).all() and np.isfinite(g["lse"]).all()
-    r = _gpu.compare(p, g)
+    out, lse = _gpu.host(g)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    _gpu.compare(p, g)
     if lam == 0:
         assert not g["bitmap"].any()
 
@@ -49,7 +51,8 @@ def test_planted_golden(lam, causal, L):
 def test_small_cases(key, lam, causal):
     p = _cases.small_problem(key)
     g = _gpu.run(p, lam=lam, causal=causal)
-    assert np.isfinite(g["out"]).all() and np.isfinite(g["lse"]).all()
+    out, lse = _gpu.host(g)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
     _gpu.compare(p, g)
 
 
@@ -57,7 +60,7 @@ def test_deterministic():
     p = _cases.small_problem("weak_sink")
     a = _gpu.run(p, lam=0.05)
     b = _gpu.run(p, lam=0.05)
-    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["lse"], b["lse"])
+    assert torch.equal(a["out"], b["out"]) and torch.equal(a["lse"], b["lse"])
     assert np.array_equal(a["bitmap"], b["bitmap"])
 
 
@@ -71,5 +74,5 @@ def test_packed_equals_separate():
         one = gi.Problem("one", p.q[a:b], p.k[a:b], p.v[a:b], np.array([0, b - a], np.int32),
                          p.Hq, p.Hkv, p.d, True, 0.01)
         g = _gpu.run(one, lam=0.01)
-        assert np.array_equal(g["out"], whole["out"][a:b])
-        assert np.array_equal(g["lse"], whole["lse"][:, a:b])
+        assert torch.equal(g["out"], whole["out"][a:b])
+        assert torch.equal(g["lse"], whole["lse"][:, a:b])
