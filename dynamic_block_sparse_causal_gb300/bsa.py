@@ -41,6 +41,8 @@ def lib() -> ctypes.CDLL:
     vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
     L.bsa_prefill_fwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp, vp]
     L.bsa_prefill_fwd.restype = i32
+    L.bsa_prefill_fwd_noalloc.argtypes = L.bsa_prefill_fwd.argtypes
+    L.bsa_prefill_fwd_noalloc.restype = i32
     L.bsa_set_fp8_scales.argtypes = [vp, vp, vp]
     L.bsa_set_fp8_scales.restype = i32
     L.bsa_quantize_fp8.argtypes = [vp, i64, i32, i32, vp, vp, vp]
@@ -83,6 +85,16 @@ def prefill_fwd(q, k, v, cu_seqlens, n_seqs, Hq, Hkv, d, causal, lam, dtype, out
     return lib().bsa_prefill_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), int(n_seqs),
                                  int(Hq), int(Hkv), int(d), int(causal), float(lam), int(dtype),
                                  _ptr(out), _ptr(lse), _ptr(skip_bitmap), _stream(stream))
+
+
+def prefill_fwd_noalloc(q, k, v, cu_seqlens, n_seqs, Hq, Hkv, d, causal, lam, dtype, out, lse,
+                        skip_bitmap, stream=None) -> int:
+    """bsa_prefill_fwd_noalloc: same call, scratch from a fixed array in the
+    library instead of an allocation (for callers that may not allocate)."""
+    return lib().bsa_prefill_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), int(n_seqs),
+                                         int(Hq), int(Hkv), int(d), int(causal), float(lam),
+                                         int(dtype), _ptr(out), _ptr(lse), _ptr(skip_bitmap),
+                                         _stream(stream))
 
 
 def set_fp8_scales(q_scale, k_scale, v_scale) -> int:

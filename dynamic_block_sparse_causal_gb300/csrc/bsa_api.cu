@@ -109,6 +109,15 @@ bool encode_tile_map(CUtensorMap *m, const void *base, int H, bool fp8) {
 
 }  // namespace
 
+namespace bsa {
+// FP8 scales set on the calling thread (for other translation units).
+void current_fp8_scales(const float **q, const float **k, const float **v) {
+  *q = t_q_scale;
+  *k = t_k_scale;
+  *v = t_v_scale;
+}
+}  // namespace bsa
+
 extern "C" {
 
 bsa_status_t bsa_prefill_fwd(const void *q, const void *k, const void *v,

@@ -76,6 +76,9 @@ cudaError_t launch_forward(const FwdParams &p, bool fp8, int num_ctas, cudaStrea
 size_t forward_smem_bytes();
 cudaError_t prepare_forward();   // per device: opt in to the shared-memory size
 
+// FP8 scales registered on the calling thread (bsa_api.cu).
+void current_fp8_scales(const float **q, const float **k, const float **v);
+
 // FP8 quantiser (bsa_quant.cu).
 cudaError_t launch_quantize_fp8(const void *x, int64_t tokens, int H, int d, uint8_t *codes,
                                 float *scale, cudaStream_t stream);

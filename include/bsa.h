@@ -106,6 +106,34 @@ bsa_status_t bsa_prefill_fwd(const void *q, const void *k, const void *v,
                              bsa_stream_t stream);
 
 /*
+ * Same forward pass as bsa_prefill_fwd, same arguments and results, for
+ * callers that may not allocate device memory -- for example a serving
+ * engine that reserves nearly all of HBM for its own pool up front and
+ * forbids allocations inside kernels' host calls, where a surprise
+ * allocation could fail or stall the device. The pages have no counterpart:
+ * this is an interface variant, not part of the method.
+ *
+ * Allocates nothing: its scratch (work queue, tensor maps, scheduling
+ * tables) is a fixed array of about 270 KiB compiled into the library and
+ * resident on every GPU that loads it until the process exits. Limit:
+ * n_seqs <= 1024 (larger batches return BSA_ERR_INVALID_ARG); sequences
+ * longer than 8M tokens are rejected on the device as with bsa_prefill_fwd.
+ * The first call on a device looks up that device's address of the array
+ * (and sets the kernel's shared-memory limit); make that first call before
+ * any stream capture. All calls share the one array and each call rewrites
+ * it: calls whose GPU work overlaps (on different streams) race and must
+ * not be issued; calls on one stream are safe. Device-side errors are not
+ * reported by bsa_get_device_status; a malformed cu_seqlens leaves the
+ * outputs unwritten.
+ */
+bsa_status_t bsa_prefill_fwd_noalloc(const void *q, const void *k, const void *v,
+                                     const int32_t *cu_seqlens, int32_t n_seqs,
+                                     int32_t Hq, int32_t Hkv, int32_t d,
+                                     int32_t causal, float lambda,
+                                     bsa_dtype_t dtype, void *out, float *lse,
+                                     uint32_t *skip_bitmap, bsa_stream_t stream);
+
+/*
  * Per-head dequantisation scales for the next BSA_FP8_E4M3 calls made on this
  * host thread: device float32 arrays q_scale [Hq], k_scale [Hkv],
  * v_scale [Hkv]; a stored code x8 stands for x8 * scale. The pointers are
