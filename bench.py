@@ -308,6 +308,36 @@ def gpu_arm(args, rank, world, local_rank):
                           "executed_tflops": round(executed_flops(seqlens, Hq, sk, d) / m / 1e9, 1),
                           "skip_fraction": round(sk / ctiles, 5)})
 
+    # dense causal attention from the box's library (torch SDPA) on the same
+    # shape: the comparison for the lambda = 0 path
+    dense_ref = None
+    if not args.no_sweep and p.n_seqs == 1:
+        try:
+            import torch.nn.functional as F
+            Q = q.view(1, T, Hq, d).transpose(1, 2)
+            K = k.view(1, T, Hkv, d).transpose(1, 2)
+            V = v.view(1, T, Hkv, d).transpose(1, 2)
+
+            def sdpa():
+                return F.scaled_dot_product_attention(Q, K, V, is_causal=True, enable_gqa=True)
+            for _ in range(2):
+                o_ref = sdpa()
+            torch.cuda.synchronize()
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n_ref = max(2, args.steps // 2)
+            ev0.record(stream)
+            for _ in range(n_ref):
+                o_ref = sdpa()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            m = ev0.elapsed_time(ev1) / n_ref
+            dense_ref = {"impl": "torch.nn.functional.scaled_dot_product_attention (is_causal, GQA)",
+                         "ms": round(m, 3), "dense_tflops": round(dflops / m / 1e9, 1),
+                         "frac_of_peak": round(dflops / m / 1e9 / peak, 4)}
+            del o_ref
+        except Exception as e:  # a missing backend is reported, not fatal
+            dense_ref = {"impl": "torch SDPA", "error": str(e)[:200]}
+
     # end to end through the C interface with host buffers
     e2e = None
     if not args.no_e2e:
@@ -365,7 +395,7 @@ def gpu_arm(args, rank, world, local_rank):
         "skip_fraction": round(skipped / ctiles, 5), "executed_tflop_per_step": round(xflops / 1e12, 3),
         "dense_equiv_tflop_per_step": round(dflops / 1e12, 3),
         "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
-        "gpu_launches": 2 * args.steps, "lambda_sweep": sweep,
+        "gpu_launches": 2 * args.steps, "lambda_sweep": sweep, "dense_reference": dense_ref,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

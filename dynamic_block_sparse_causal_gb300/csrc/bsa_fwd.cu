@@ -13,9 +13,10 @@
 //    first, builds the work-item level table and the skip-bitmap offsets,
 //    and writes the TMA tensor maps with the token extent patched in.
 //  * fwd_kernel<FP8> (persistent, one CTA per SM, 384 threads):
-//      warp 0  lane 0   TMA producer: Q tiles, then the K ring (2 stages)
-//      warp 1  lane 0   tcgen05 MMA issuer; also issues the V load of a tile
-//                       once one of the two query tiles votes to keep it
+//      warp 0  lane 0   TMA producer: Q tiles, the K ring (3 stages), and,
+//                       when skipping is off, V with every K
+//      warp 1  lane 0   tcgen05 MMA issuer; with skipping on it also requests
+//                       V_j (2-stage ring) as soon as a query tile votes to keep j
 //      warp 2  lane 0   fetches the next work item (atomic counter)
 //      warps 4-7        softmax warpgroup of query slot 0 (TMEM lanes 0-127)
 //      warps 8-11       softmax warpgroup of query slot 1
@@ -24,15 +25,18 @@
 //    tile loaded feeds two QK^T MMAs.
 //
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512),
-// fp32, lane = query row. Shared memory (1024-aligned, 128-byte swizzle):
-// Q0 Q1 K[2] V P0 P1, 32 KiB each.
+// fp32, lane = query row; P_s (bf16 / e4m3) is written over the first
+// columns of S_s and read from there by the P.V MMA. Shared memory
+// (1024-aligned, 128-byte swizzle): Q0 Q1 K[3] V[2], 32 KiB each.
 //
 // Per key tile j and query slot s the softmax warpgroup loads S_s from TMEM,
-// masks the diagonal / tail, takes the row max, and votes with bar.red.and.
-// A skipped tile releases S_s at once; a kept tile updates the running max
-// (lazy rescale of O when the reference max grows by more than 2^8),
-// writes P = exp2(S c - m_ref) as bf16 (e4m3) into shared memory and hands
-// it to the MMA warp, which only then requests V_j.
+// masks the diagonal / tail, takes the row max, and votes with one
+// bar.red.and. The vote is posted at once: a skipped tile frees S_s for the
+// next QK^T; a kept tile lets the MMA warp request V_j while the warpgroup
+// computes P = exp2(S c - m_ref) (lazy O rescale when the reference max
+// grows by more than 2^8) into TMEM and then posts P-ready. The MMA warp
+// issues O_s += P_s V_j before the next S_s, so the tensor pipe's in-order
+// execution protects P until it has been read.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -136,18 +140,29 @@ cudaError_t launch_prologue(const int32_t *cu_seqlens, int n_seqs, int Hq, int H
 
 namespace {
 
-constexpr uint32_t kRegion = 32768;   // one tile slot in shared memory
+constexpr uint32_t kRegion = 32768;   // one bf16 tile slot in shared memory
 constexpr uint32_t kBox = 16384;      // one 128-row x 128-byte TMA box
-constexpr uint32_t SM_Q0 = 0, SM_Q1 = kRegion, SM_K = 2 * kRegion, SM_V = 4 * kRegion,
-                   SM_P0 = 5 * kRegion, SM_P1 = 6 * kRegion, SM_BYTES = 7 * kRegion;
-constexpr int kStages = 2;
+constexpr int kKStages = 3;           // K ring depth
+constexpr int kVStages = 2;           // V ring depth
+constexpr uint32_t SM_Q0 = 0, SM_Q1 = kRegion, SM_K = 2 * kRegion,
+                   SM_V = SM_K + kKStages * kRegion, SM_BYTES = SM_V + kVStages * kRegion;
 constexpr float kRescaleLog2 = 8.0f;  // lazy O rescale once m grows by 2^8
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint32_t kColS = 0, kColO = 256;   // TMEM: S_s at s*128, O_s at 256 + s*128
 
 // barrier slots
 enum : int {
-  B_Q = 0, B_KF = 1, B_KE = B_KF + kStages, B_VF = B_KE + kStages, B_VE, B_SF, B_DEC = B_SF + 2,
-  B_PV = B_DEC + 2, B_DRAIN = B_PV + 2, B_COUNT
+  B_Q = 0,
+  B_KF = 1,
+  B_KE = B_KF + kKStages,
+  B_VF = B_KE + kKStages,
+  B_VE = B_VF + kVStages,
+  B_SF = B_VE + kVStages,   // S_s computed (per slot)
+  B_VOTE = B_SF + 2,        // slot s voted on the tile (S_s free if skipped)
+  B_PRDY = B_VOTE + 2,      // P_s written to TMEM (S_s consumed)
+  B_PV = B_PRDY + 2,        // O_s += P_s V done
+  B_DRAIN = B_PV + 2,
+  B_COUNT
 };
 
 template <bool FP8>
@@ -176,27 +191,22 @@ __device__ __forceinline__ void issue_qk(uint32_t d, uint32_t qs, uint32_t ks) {
   }
 }
 
-// O += P V: A = P (K-major over keys), B = V as stored (keys x head dim,
-// head dim contiguous) = MN-major; 8-row groups of keys 1024 bytes apart,
+// O += P V: A = P from TMEM (row = lane, two bf16 or four e4m3 keys per
+// 32-bit column, so every K step is 8 columns), B = V as stored (keys x head
+// dim, head dim contiguous) = MN-major; 8-row key groups 1024 bytes apart,
 // the two 64-column halves of a bf16 V tile 16 KiB apart.
 template <bool FP8>
-__device__ __forceinline__ void issue_pv(uint32_t d, uint32_t ps, uint32_t vs, bool acc) {
+__device__ __forceinline__ void issue_pv(uint32_t d, uint32_t p_tmem, uint32_t vs, bool acc) {
 #pragma unroll
   for (int kk = 0; kk < Cfg<FP8>::kSteps; ++kk) {
-    const uint32_t aoff = FP8 ? kk * 32 : (kk >> 2) * kBox + (kk & 3) * 32;
     const uint32_t boff = FP8 ? kk * 4096 : kk * 2048;
-    const uint64_t a = sdesc_sw128(ps + aoff, 16, 1024);
     const uint64_t b = sdesc_sw128(vs + boff, kBox, 1024);
     if (FP8)
-      mma_f8_ss(d, a, b, Cfg<FP8>::kIdescPV, (kk > 0 || acc) ? 1u : 0u);
+      mma_f8_ts(d, p_tmem + kk * 8, b, Cfg<FP8>::kIdescPV, (kk > 0 || acc) ? 1u : 0u);
     else
-      mma_f16_ss(d, a, b, Cfg<FP8>::kIdescPV, (kk > 0 || acc) ? 1u : 0u);
+      mma_f16_ts(d, p_tmem + kk * 8, b, Cfg<FP8>::kIdescPV, (kk > 0 || acc) ? 1u : 0u);
   }
 }
-
-struct Item {
-  int valid, s, kvh, h0, h1, qi, a, L;
-};
 
 __device__ void fetch_item(const FwdParams &p, int total_items, int maxn, int *dst) {
   const int k = atomicAdd(&p.ws->counter, 1);
@@ -229,6 +239,31 @@ __device__ void fetch_item(const FwdParams &p, int total_items, int maxn, int *d
   dst[7] = p.cu_seqlens[s + 1] - a;
 }
 
+// Running row max over two 32-register chunks (three-input max, eight
+// independent chains).
+__device__ __forceinline__ void row_max64(float (&a)[8], const uint32_t (&v0)[32],
+                                          const uint32_t (&v1)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 16) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      a[k] = max3f(a[k], __uint_as_float(v0[i + 2 * k]), __uint_as_float(v0[i + 2 * k + 1]));
+      a[k] = max3f(a[k], __uint_as_float(v1[i + 2 * k]), __uint_as_float(v1[i + 2 * k + 1]));
+    }
+  }
+}
+
+// -inf on the masked columns of one 32-column chunk: keys past the query
+// (diagonal tile) or past the sequence end (tail tile, non-causal).
+__device__ __forceinline__ void mask_chunk(uint32_t (&v)[32], int ch, bool diag, bool tailt,
+                                           int row, int key0, int L) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const int col = ch * 32 + e;
+    if ((diag && col > row) || (tailt && key0 + col >= L)) v[e] = __float_as_uint(-INFINITY);
+  }
+}
+
 }  // namespace
 
 template <bool FP8>
@@ -238,8 +273,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   __shared__ uint64_t bar[B_COUNT];
   __shared__ uint32_t tmem_sh;
   __shared__ int item_sh[2][8];
-  __shared__ volatile int dec_sh[2];
-  __shared__ int abort_sh;
+  __shared__ volatile int vote_sh[2];
+  __shared__ volatile int abort_sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t raw = smem_u32(smem_raw);
@@ -248,6 +283,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   Workspace *ws = p.ws;
   const int total_items = ws->total_items, maxn = ws->max_tiles, T = ws->total_tokens;
   const uint64_t limit = p.wait_limit_ns;
+  const bool v_prefetch = !(p.log2_lambda > -INFINITY);   // no skipping: V streams with K
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < B_COUNT; ++b) mbar_init(&bar[b], 1);
@@ -270,15 +306,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   const uint32_t tmem = tmem_sh;
 
   // pipeline counters, persistent across items (each role keeps its own)
-  uint32_t kc = 0, vc = 0, qc = 0, dc0 = 0, dc1 = 0, sc = 0, pvc = 0;
-  int kc_last[kStages] = {-1, -1};
-  int vc_last = -1, qc_last = -1;
+  uint32_t kc = 0, vc = 0, qc = 0, vt0 = 0, vt1 = 0, pr0 = 0, pr1 = 0, sc = 0, pvc = 0;
+  int kc_last[kKStages] = {-1, -1, -1};
+  int vc_last[kVStages] = {-1, -1};
+  int qc_last = -1;
 
   for (int it = 0;; ++it) {
     const int *I = item_sh[it & 1];
     if (!I[0] || abort_sh) break;
-    const int kvh = I[2], h0 = I[3], h1 = I[4], qi = I[5], a = I[6], L = I[7];
-    const int s = I[1];
+    const int s = I[1], kvh = I[2], h0 = I[3], h1 = I[4], qi = I[5], a = I[6], L = I[7];
     const int n = (L + kTile - 1) / kTile;
     const int last = p.causal ? qi : n - 1;
     const bool has1 = h1 >= 0;
@@ -287,7 +323,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     if (warp == 0) {
       if (lane == 0) {
         // ------------------------------------------------ TMA producer
-        const void *tq = &ws->tmap[0], *tk = &ws->tmap[1];
+        const void *tq = &ws->tmap[0], *tk = &ws->tmap[1], *tv = &ws->tmap[2];
         mbar_expect_tx(&bar[B_Q], (has1 ? 2 : 1) * C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b) {
           tma_load_3d(sptr + SM_Q0 + b * kBox, tq, &bar[B_Q], b * C::kBoxCols, h0, a + qi * kTile);
@@ -297,8 +333,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         }
         qc_last = (int)qc++;
         for (int j = 0; j <= last && ok; ++j) {
-          const uint32_t st = kc % kStages;
-          ok = mbar_wait(&bar[B_KE + st], ((kc / kStages) & 1) ^ 1, limit);
+          const uint32_t st = kc % kKStages;
+          ok = mbar_wait(&bar[B_KE + st], ((kc / kKStages) & 1) ^ 1, limit);
           if (!ok) break;
           if ((int)kc != p.debug_drop_k_load) {
             mbar_expect_tx(&bar[B_KF + st], C::kTileBytes);
@@ -308,30 +344,45 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             kc_last[st] = (int)kc;
           }
           ++kc;
+          if (v_prefetch) {
+            const uint32_t vs = vc % kVStages;
+            ok = mbar_wait(&bar[B_VE + vs], ((vc / kVStages) & 1) ^ 1, limit);
+            if (!ok) break;
+            mbar_expect_tx(&bar[B_VF + vs], C::kTileBytes);
+            for (int b = 0; b < C::kBoxes; ++b)
+              tma_load_3d(sptr + SM_V + vs * kRegion + b * kBox, tv, &bar[B_VF + vs],
+                          b * C::kBoxCols, kvh, a + j * kTile);
+            vc_last[vs] = (int)vc;
+            ++vc;
+          }
         }
       }
     } else if (warp == 1) {
       if (lane == 0) {
         // ------------------------------------------------ MMA issuer
         const void *tv = &ws->tmap[2];
-        const uint32_t S0 = tmem, S1 = tmem + 128, O0 = tmem + 256, O1 = tmem + 384;
-        const uint32_t q0s = sbase + SM_Q0, q1s = sbase + SM_Q1, vs = sbase + SM_V;
-        const uint32_t p0s = sbase + SM_P0, p1s = sbase + SM_P1;
+        const uint32_t S0 = tmem + kColS, S1 = tmem + kColS + 128;
+        const uint32_t O0 = tmem + kColO, O1 = tmem + kColO + 128;
+        const uint32_t q0s = sbase + SM_Q0, q1s = sbase + SM_Q1;
+        // V_j request from this thread (skipping on): only kept tiles are loaded
         auto issue_v = [&](int j) -> bool {
-          if (!mbar_wait(&bar[B_VE], (vc & 1) ^ 1, limit)) return false;
-          mbar_expect_tx(&bar[B_VF], C::kTileBytes);
+          const uint32_t vs = vc % kVStages;
+          if (!mbar_wait(&bar[B_VE + vs], ((vc / kVStages) & 1) ^ 1, limit)) return false;
+          mbar_expect_tx(&bar[B_VF + vs], C::kTileBytes);
           for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(sptr + SM_V + b * kBox, tv, &bar[B_VF], b * C::kBoxCols, kvh,
-                        a + j * kTile);
-          vc_last = (int)vc;
+            tma_load_3d(sptr + SM_V + vs * kRegion + b * kBox, tv, &bar[B_VF + vs],
+                        b * C::kBoxCols, kvh, a + j * kTile);
+          vc_last[vs] = (int)vc;
           return true;
         };
         do {
+          // key tile 0 is never skipped: request its V before anything else
+          if (!v_prefetch && !(ok = issue_v(0))) break;
           ok = mbar_wait(&bar[B_Q], qc & 1, limit);
           ++qc;
           if (!ok) break;
-          uint32_t st = kc % kStages;
-          ok = mbar_wait(&bar[B_KF + st], (kc / kStages) & 1, limit);
+          uint32_t st = kc % kKStages;
+          ok = mbar_wait(&bar[B_KF + st], (kc / kKStages) & 1, limit);
           if (!ok) break;
           tc_fence_after();
           uint32_t ks = sbase + SM_K + st * kRegion;
@@ -345,35 +396,57 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           ++kc;
           bool oinit0 = false, oinit1 = false;
           for (int j = 0; j <= last && ok; ++j) {
-            bool v_issued = false;
-            ok = mbar_wait(&bar[B_DEC + 0], dc0 & 1, limit);
-            ++dc0;
+            bool vload = v_prefetch || j == 0;   // V_j requested
+            bool vready = false;                 // V_j landed (waited)
+            const uint32_t vs = vc % kVStages;
+            auto wait_v = [&]() -> bool {
+              if (vready) return true;
+              if (!mbar_wait(&bar[B_VF + vs], (vc / kVStages) & 1, limit)) return false;
+              tc_fence_after();
+              vready = true;
+              return true;
+            };
+            // ---- slot 0: vote, then P.V (if kept) before the next S overwrites P
+            ok = mbar_wait(&bar[B_VOTE + 0], vt0 & 1, limit);
+            ++vt0;
             if (!ok) break;
-            tc_fence_after();
-            const bool skip0 = dec_sh[0] != 0;
-            if (!skip0) {
-              if (!(ok = issue_v(j))) break;
-              v_issued = true;
+            const bool keep0 = vote_sh[0] == 0;
+            if (keep0) {
+              if (!vload && !(ok = issue_v(j))) break;
+              vload = true;
+              ok = mbar_wait(&bar[B_PRDY + 0], pr0 & 1, limit);
+              ++pr0;
+              if (!ok || !(ok = wait_v())) break;
+              tc_fence_after();
+              issue_pv<FP8>(O0, S0, sbase + SM_V + vs * kRegion, oinit0);
+              oinit0 = true;
+              mma_commit(&bar[B_PV + 0]);
             }
             if (j < last) {
-              st = kc % kStages;
-              ok = mbar_wait(&bar[B_KF + st], (kc / kStages) & 1, limit);
+              st = kc % kKStages;
+              ok = mbar_wait(&bar[B_KF + st], (kc / kKStages) & 1, limit);
               if (!ok) break;
               tc_fence_after();
               ks = sbase + SM_K + st * kRegion;
               issue_qk<FP8>(S0, q0s, ks);
               mma_commit(&bar[B_SF + 0]);
             }
-            bool skip1 = true;
+            // ---- slot 1
             if (has1) {
-              ok = mbar_wait(&bar[B_DEC + 1], dc1 & 1, limit);
-              ++dc1;
+              ok = mbar_wait(&bar[B_VOTE + 1], vt1 & 1, limit);
+              ++vt1;
               if (!ok) break;
-              tc_fence_after();
-              skip1 = dec_sh[1] != 0;
-              if (!skip1 && !v_issued) {
-                if (!(ok = issue_v(j))) break;
-                v_issued = true;
+              const bool keep1 = vote_sh[1] == 0;
+              if (keep1) {
+                if (!vload && !(ok = issue_v(j))) break;
+                vload = true;
+                ok = mbar_wait(&bar[B_PRDY + 1], pr1 & 1, limit);
+                ++pr1;
+                if (!ok || !(ok = wait_v())) break;
+                tc_fence_after();
+                issue_pv<FP8>(O1, S1, sbase + SM_V + vs * kRegion, oinit1);
+                oinit1 = true;
+                mma_commit(&bar[B_PV + 1]);
               }
               if (j < last) {
                 issue_qk<FP8>(S1, q1s, ks);
@@ -384,21 +457,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
               mma_commit(&bar[B_KE + st]);
               ++kc;
             }
-            if (v_issued) {
-              ok = mbar_wait(&bar[B_VF], vc & 1, limit);
-              if (!ok) break;
-              tc_fence_after();
-              if (!skip0) {
-                issue_pv<FP8>(O0, p0s, vs, oinit0);
-                oinit0 = true;
-                mma_commit(&bar[B_PV + 0]);
-              }
-              if (!skip1) {
-                issue_pv<FP8>(O1, p1s, vs, oinit1);
-                oinit1 = true;
-                mma_commit(&bar[B_PV + 1]);
-              }
-              mma_commit(&bar[B_VE]);
+            if (vload) {   // keep the V ring in step even if nobody used the tile
+              if (!(ok = wait_v())) break;
+              mma_commit(&bar[B_VE + vs]);
               ++vc;
             }
           }
@@ -414,9 +475,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         const int row = threadIdx.x - 128 * (slot + 1);   // 0..127 = TMEM lane
         const uint32_t barid = 1 + slot;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + slot * 128 + lane_off;
-        const uint32_t tO = tmem + 256 + slot * 128 + lane_off;
-        const uint32_t ps = sbase + (slot ? SM_P1 : SM_P0);
+        const uint32_t tS = tmem + kColS + slot * 128 + lane_off;
+        const uint32_t tO = tmem + kColO + slot * 128 + lane_off;
         const int qpos = qi * kTile + row;
         const bool valid = qpos < L;
         const bool tail = !p.causal && (L % kTile) != 0;
@@ -426,64 +486,58 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         const long long boff = p.seq_bitmap_off[s] + ((long long)h * n + qi) * W;
         float m2 = -INFINITY, mref = 0.f, l = 0.f;
         uint32_t word = 0;
-        bool pv_pending = false, have_kept = false;
+        bool have_kept = false;
 
         for (int j = 0; j <= last; ++j) {
-          bool wok = true;
-          if (row == 0) wok = mbar_wait(&bar[B_SF + slot], sc & 1, limit);
+          if (!mbar_wait(&bar[B_SF + slot], sc & 1, limit)) abort_sh = 1;
           ++sc;
-          if (bar_red_or(!wok, barid, 128)) {
-            ok = false;
-            break;
-          }
           tc_fence_after();
           const bool diag = p.causal && j == qi;
           const bool tailt = tail && j == n - 1;
-          const bool masked_tile = diag || tailt;
-          float rm = -INFINITY;
+          float rm;
+          {
+            float acc[8];
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t v[32];
-            tmem_ld32(tS + ch * 32, v);
-            tmem_wait_ld(v);
-            if (masked_tile) {
+            for (int k = 0; k < 8; ++k) acc[k] = -INFINITY;
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const int col = ch * 32 + e;
-                const bool msk = (diag && col > row) || (tailt && j * kTile + col >= L);
-                rm = fmaxf(rm, msk ? -INFINITY : __uint_as_float(v[e]));
+            for (int half = 0; half < 2; ++half) {
+              uint32_t v0[32], v1[32];
+              tmem_ld32(tS + half * 64, v0);
+              tmem_ld32(tS + half * 64 + 32, v1);
+              tmem_wait_ld(v0);
+              reg_fence(v1);
+              if (diag || tailt) {
+                mask_chunk(v0, 2 * half, diag, tailt, row, j * kTile, L);
+                mask_chunk(v1, 2 * half + 1, diag, tailt, row, j * kTile, L);
               }
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) rm = fmaxf(rm, __uint_as_float(v[e]));
+              row_max64(acc, v0, v1);
             }
+            rm = max3f(max3f(acc[0], acc[1], acc[2]), max3f(acc[3], acc[4], acc[5]),
+                       fmaxf(acc[6], acc[7]));
           }
           const float trm = rm * c;
           const bool pred = !valid || (trm < m2 + p.log2_lambda);
           tc_fence_before();
           const bool skip = bar_red_and(pred, barid, 128);
+          if (abort_sh) {   // read after the barrier: uniform over the warpgroup
+            ok = false;
+            break;
+          }
+          if (row == 0) {
+            vote_sh[slot] = skip ? 1 : 0;
+            mbar_arrive(&bar[B_VOTE + slot]);
+          }
           if (skip) {
-            if (row == 0) {
-              word |= 1u << (j & 31);
-              dec_sh[slot] = 1;
-              mbar_arrive(&bar[B_DEC + slot]);
-            }
+            if (row == 0) word |= 1u << (j & 31);
           } else {
             const float mnew = valid ? fmaxf(m2, trm) : 0.f;
-            if (pv_pending) {  // P buffer and O are still in use by the last P.V
-              bool pok = true;
-              if (row == 0) pok = mbar_wait(&bar[B_PV + slot], pvc & 1, limit);
+            if (have_kept) {
+              // the previous P.V of this slot is complete by now (it was issued
+              // before this tile's S); waiting keeps the phase count exact and
+              // orders the O rescale after it
+              if (!mbar_wait(&bar[B_PV + slot], pvc & 1, limit)) abort_sh = 1;
               ++pvc;
-              pv_pending = false;
-              if (bar_red_or(!pok, barid, 128)) {
-                ok = false;
-                break;
-              }
               tc_fence_after();
-            }
-            if (!have_kept) {
-              mref = mnew;
-            } else {
               const bool need = valid && (mnew - mref > kRescaleLog2);
               if (__any_sync(0xffffffffu, need)) {
                 const float alpha = need ? ex2_approx(mref - mnew) : 1.f;
@@ -499,23 +553,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
                     v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
                   tmem_st32(tO + ch * 32, v);
                 }
-                tmem_wait_st();
               }
+            } else {
+              mref = mnew;
             }
             m2 = mnew;
+            // P = exp2(S c - m_ref), written over the S columns already read:
+            // chunk ch (keys 32ch..32ch+31) goes to columns 16ch.. (bf16) or 8ch.. (e4m3)
             float sum = 0.f;
+            const float nm = -mref;
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
               uint32_t v[32];
               tmem_ld32(tS + ch * 32, v);
               tmem_wait_ld(v);
+              if (diag || tailt) mask_chunk(v, ch, diag, tailt, row, j * kTile, L);
               float pe[32];
 #pragma unroll
               for (int e = 0; e < 32; ++e) {
-                const int col = ch * 32 + e;
-                const bool msk = !valid || (masked_tile && ((diag && col > row) ||
-                                                           (tailt && j * kTile + col >= L)));
-                pe[e] = msk ? 0.f : ex2_approx(fmaf(__uint_as_float(v[e]), c, -mref));
+                pe[e] = valid ? ex2_approx(fmaf(__uint_as_float(v[e]), c, nm)) : 0.f;
                 sum += pe[e];
               }
               if (FP8) {
@@ -524,33 +580,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
                 for (int k = 0; k < 8; ++k)
                   w8[k] = (uint32_t)pack_e4m3x2(pe[4 * k], pe[4 * k + 1]) |
                           ((uint32_t)pack_e4m3x2(pe[4 * k + 2], pe[4 * k + 3]) << 16);
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                  const uint32_t u = 2 * ch + q;
-                  st_shared_v4(ps + row * 128 + ((u ^ (row & 7)) << 4), w8[4 * q], w8[4 * q + 1],
-                               w8[4 * q + 2], w8[4 * q + 3]);
-                }
+                tmem_st8(tS + ch * 8, w8);
               } else {
                 uint32_t w2[16];
 #pragma unroll
                 for (int k = 0; k < 16; ++k) w2[k] = pack_bf16x2(pe[2 * k], pe[2 * k + 1]);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  const uint32_t u = (ch & 1) * 4 + q;
-                  st_shared_v4(ps + (ch >> 1) * kBox + row * 128 + ((u ^ (row & 7)) << 4),
-                               w2[4 * q], w2[4 * q + 1], w2[4 * q + 2], w2[4 * q + 3]);
-                }
+                tmem_st16(tS + ch * 16, w2);
               }
             }
+            tmem_wait_st();
             l += sum;
-            fence_proxy_async_smem();
             tc_fence_before();
             named_bar_sync(barid, 128);
-            if (row == 0) {
-              dec_sh[slot] = 0;
-              mbar_arrive(&bar[B_DEC + slot]);
+            if (abort_sh) {
+              ok = false;
+              break;
             }
-            pv_pending = true;
+            if (row == 0) mbar_arrive(&bar[B_PRDY + slot]);
             have_kept = true;
           }
           if (row == 0 && p.bitmap && (((j & 31) == 31) || j == last)) {
@@ -559,13 +605,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           }
         }
         // ------------------------------------------------ epilogue
-        if (ok && pv_pending) {
-          bool pok = true;
-          if (row == 0) pok = mbar_wait(&bar[B_PV + slot], pvc & 1, limit);
+        if (ok && have_kept) {
+          if (!mbar_wait(&bar[B_PV + slot], pvc & 1, limit)) abort_sh = 1;
           ++pvc;
-          if (bar_red_or(!pok, barid, 128)) ok = false;
-        }
-        if (ok) {
           tc_fence_after();
           float inv = 0.f;
           if (valid && l > 0.f) inv = (FP8 ? p.v_scale[kvh] : 1.f) / l;
@@ -579,7 +621,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             uint32_t w2[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k)
-              w2[k] = pack_bf16x2(__uint_as_float(v[2 * k]) * inv, __uint_as_float(v[2 * k + 1]) * inv);
+              w2[k] = pack_bf16x2(__uint_as_float(v[2 * k]) * inv,
+                                  __uint_as_float(v[2 * k + 1]) * inv);
             if (valid) {
               uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
 #pragma unroll
@@ -593,25 +636,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         }
       }
     }
-    if (!ok) {
-      abort_sh = 1;
-      atomicOr(&ws->status, kStatusTimeout);
-    }
+    if (!ok) abort_sh = 1;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (abort_sh && threadIdx.x == 0) atomicOr(&ws->status, kStatusTimeout);
   }
 
   // Normal exit: every item ended fully drained. After a time-out, wait
   // (bounded) for this CTA's own copies and MMAs before giving TMEM back.
   if (abort_sh) {
-    if (warp == 0 && lane == 0) {
-      for (int st = 0; st < kStages; ++st)
-        if (kc_last[st] >= 0) mbar_wait(&bar[B_KF + st], (kc_last[st] / kStages) & 1, limit);
-      if (qc_last >= 0) mbar_wait(&bar[B_Q], qc_last & 1, limit);
+    if ((warp == 0 || warp == 1) && lane == 0) {
+      for (int st = 0; st < kKStages; ++st)
+        if (warp == 0 && kc_last[st] >= 0)
+          mbar_wait(&bar[B_KF + st], (kc_last[st] / kKStages) & 1, limit);
+      for (int st = 0; st < kVStages; ++st)
+        if (vc_last[st] >= 0) mbar_wait(&bar[B_VF + st], (vc_last[st] / kVStages) & 1, limit);
+      if (warp == 0 && qc_last >= 0) mbar_wait(&bar[B_Q], qc_last & 1, limit);
     }
     if (warp == 1 && lane == 0) {
-      if (vc_last >= 0) mbar_wait(&bar[B_VF], vc_last & 1, limit);
       mma_commit(&bar[B_DRAIN]);
       mbar_wait(&bar[B_DRAIN], 0, limit);
     }
@@ -636,7 +679,8 @@ cudaError_t launch_forward(const FwdParams &p, bool fp8, int num_ctas, cudaStrea
 
 cudaError_t prepare_forward() {
   const int smem = (int)forward_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
