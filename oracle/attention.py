@@ -27,11 +27,14 @@ import numpy as np
 
 
 def dense(q: np.ndarray, k: np.ndarray, v: np.ndarray, cu_seqlens, Hq: int, Hkv: int,
-          causal: bool = True, scale: float | None = None, allowed=None, heads=None):
+          causal: bool = True, scale: float | None = None, allowed=None, heads=None,
+          cu_seqlens_k=None):
     """Return ``(out [T, Hq, d], lse [Hq, T])`` as float64.
 
     q, k, v are float64 ``[T, H, d]`` values. Rows of heads not listed in
-    ``heads`` are left as NaN.
+    ``heads`` are left as NaN. ``cu_seqlens_k`` gives separate key boundaries
+    (chunked prefill): the Lq queries of a sequence are its last Lq
+    positions, so query r may see key c when c <= Lk - Lq + r.
     """
     T, _, d = q.shape
     if scale is None:
@@ -40,24 +43,26 @@ def dense(q: np.ndarray, k: np.ndarray, v: np.ndarray, cu_seqlens, Hq: int, Hkv:
     out = np.full((T, Hq, d), np.nan)
     lse = np.full((Hq, T), np.nan)
     cu = [int(x) for x in cu_seqlens]
+    cuk = cu if cu_seqlens_k is None else [int(x) for x in cu_seqlens_k]
     for s in range(len(cu) - 1):
         a, b = cu[s], cu[s + 1]
-        L = b - a
-        if L == 0:
+        ak, bk = cuk[s], cuk[s + 1]
+        Lq, Lk = b - a, bk - ak
+        if Lq == 0:
             continue
         for h in (range(Hq) if heads is None else heads):
             g = h // G
-            S = (q[a:b, h, :] @ k[a:b, g, :].T) * scale
-            keep = np.ones((L, L), bool)
+            S = (q[a:b, h, :] @ k[ak:bk, g, :].T) * scale
+            keep = np.ones((Lq, Lk), bool)
             if causal:
-                keep &= np.tri(L, L, 0, dtype=bool)
+                keep &= np.tri(Lq, Lk, Lk - Lq, dtype=bool)
             if allowed is not None:
                 keep &= allowed(s, h)
             S = np.where(keep, S, -np.inf)
             mx = S.max(axis=1, keepdims=True)
             E = np.exp(S - mx)
             z = E.sum(axis=1, keepdims=True)
-            out[a:b, h, :] = (E / z) @ v[a:b, g, :]
+            out[a:b, h, :] = (E / z) @ v[ak:bk, g, :]
             lse[h, a:b] = (mx + np.log(z))[:, 0]
     return out, lse
 

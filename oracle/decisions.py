@@ -30,29 +30,36 @@ from . import layout
 TILE = 128
 
 
-def tile_row_max(q, k, cu_seqlens, Hq, Hkv, causal, scale, item) -> np.ndarray:
-    """``rm[j, r]``: the max score of query row r over key tile j (visited tiles)."""
+def tile_row_max(q, k, cu_seqlens, Hq, Hkv, causal, scale, item, cu_seqlens_k=None) -> np.ndarray:
+    """``rm[j, r]``: the max score of query row r over key tile j (visited tiles).
+
+    With ``cu_seqlens_k`` the queries are the last positions of their
+    sequence (chunked prefill, bottom-right causal alignment)."""
     s, h, i = item
     cu = [int(x) for x in cu_seqlens]
-    a, L = cu[s], cu[s + 1] - cu[s]
-    n = layout.tiles(L)
+    cuk = cu if cu_seqlens_k is None else [int(x) for x in cu_seqlens_k]
+    a, Lq = cu[s], cu[s + 1] - cu[s]
+    ak, Lk = cuk[s], cuk[s + 1] - cuk[s]
+    off = Lk - Lq
+    n = layout.tiles(Lk)
     g = h // (Hq // Hkv)
-    r0, r1 = i * TILE, min((i + 1) * TILE, L)
-    last = i if causal else n - 1
-    keys = np.arange(0, min((last + 1) * TILE, L))
-    S = (q[a + r0:a + r1, h, :] @ k[a + keys, g, :].T) * scale      # [rows, keys]
+    r0, r1 = i * TILE, min((i + 1) * TILE, Lq)
+    last = min((off + r1 - 1) // TILE, n - 1) if causal else n - 1
+    keys = np.arange(0, min((last + 1) * TILE, Lk))
+    S = (q[a + r0:a + r1, h, :] @ k[ak + keys, g, :].T) * scale      # [rows, keys]
     if causal:
-        S = np.where(keys[None, :] > np.arange(r0, r1)[:, None], -np.inf, S)
+        S = np.where(keys[None, :] > off + np.arange(r0, r1)[:, None], -np.inf, S)
     pad = (last + 1) * TILE - S.shape[1]
     S = np.pad(S, ((0, 0), (0, pad)), constant_values=-np.inf)
     return S.reshape(S.shape[0], last + 1, TILE).max(axis=2).T        # [tiles, rows]
 
 
-def skip_bits(q, k, cu_seqlens, Hq, Hkv, causal, lam, scale=None, item=(0, 0, 0)) -> np.ndarray:
+def skip_bits(q, k, cu_seqlens, Hq, Hkv, causal, lam, scale=None, item=(0, 0, 0),
+              cu_seqlens_k=None) -> np.ndarray:
     """Bool array over visited key tiles: True where the tile is skipped."""
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[2])
-    rm = tile_row_max(q, k, cu_seqlens, Hq, Hkv, causal, scale, item)
+    rm = tile_row_max(q, k, cu_seqlens, Hq, Hkv, causal, scale, item, cu_seqlens_k)
     if lam == 0:
         return np.zeros(rm.shape[0], bool)
     prefix = np.maximum.accumulate(rm, axis=0)

@@ -74,33 +74,47 @@ def all_items(cu_seqlens, Hq: int):
     return items
 
 
-def walk_one(q, k, v, cu_seqlens, Hq, Hkv, causal, lam, scale, item, replay=None):
+def walk_one(q, k, v, cu_seqlens, Hq, Hkv, causal, lam, scale, item, replay=None,
+             cu_seqlens_k=None):
     """Run the tile walk for one query tile; return (out rows, lse rows, bits, margins, kept).
 
     ``replay``: optional bool array over key tiles; when given, the skip
     decisions are read from it instead of computed.
+
+    ``cu_seqlens_k`` (chunked prefill): key/value sequence boundaries when they
+    differ from the queries'. Sequence s then has Lk keys and its Lq queries
+    are the last Lq positions of the sequence (query row r sits at position
+    Lk - Lq + r, bottom-right causal alignment), as when a long prompt is
+    prefilled chunk by chunk against the KV of the chunks before it (the
+    prefill-acceleration blog's §3.1 chunked prefill; FlowPrefill's chunked
+    prefill baseline). Without it, Lk = Lq and positions start at 0.
     """
     s, h, i = item
-    cu = [int(x) for x in cu_seqlens]
-    a, L = cu[s], cu[s + 1] - cu[s]
-    n = layout.tiles(L)
+    cuq = [int(x) for x in cu_seqlens]
+    cuk = cuq if cu_seqlens_k is None else [int(x) for x in cu_seqlens_k]
+    aq, Lq = cuq[s], cuq[s + 1] - cuq[s]
+    ak, Lk = cuk[s], cuk[s + 1] - cuk[s]
+    off = Lk - Lq
+    if causal and off < 0:
+        raise ValueError("causal chunked prefill needs at least as many keys as queries")
+    n = layout.tiles(Lk)
     g = h // (Hq // Hkv)
-    r0, r1 = i * TILE, min((i + 1) * TILE, L)
-    Qi = q[a + r0:a + r1, h, :]
-    qpos = np.arange(r0, r1)
+    r0, r1 = i * TILE, min((i + 1) * TILE, Lq)
+    Qi = q[aq + r0:aq + r1, h, :]
+    qpos = off + np.arange(r0, r1)
     nrow = r1 - r0
     m = np.full(nrow, -np.inf)
     l = np.zeros(nrow)
     O = np.zeros((nrow, q.shape[2]))
-    last = i if causal else n - 1
+    last = min((off + r1 - 1) // TILE, n - 1) if causal else n - 1
     ln_lam = math.log(lam) if lam > 0 else -np.inf
     bits = np.zeros(n, bool)
     margins = np.full(last + 1, -np.inf)
     kept = []
     for j in range(last + 1):
-        c0, c1 = j * TILE, min((j + 1) * TILE, L)
-        Kj = k[a + c0:a + c1, g, :]
-        Vj = v[a + c0:a + c1, g, :]
+        c0, c1 = j * TILE, min((j + 1) * TILE, Lk)
+        Kj = k[ak + c0:ak + c1, g, :]
+        Vj = v[ak + c0:ak + c1, g, :]
         S = (Qi @ Kj.T) * scale
         if causal:
             S = np.where(np.arange(c0, c1)[None, :] > qpos[:, None], -np.inf, S)
@@ -116,8 +130,9 @@ def walk_one(q, k, v, cu_seqlens, Hq, Hkv, causal, lam, scale, item, replay=None
             continue
         kept.append(j)
         m_new = np.maximum(m, rm)
-        alpha = np.exp(m - m_new)
-        P = np.exp(S - m_new[:, None])
+        with np.errstate(invalid="ignore"):
+            alpha = np.where(m_new == -np.inf, 0.0, np.exp(m - m_new))
+            P = np.where(m_new[:, None] == -np.inf, 0.0, np.exp(S - m_new[:, None]))
         l = alpha * l + P.sum(axis=1)
         O = alpha[:, None] * O + P @ Vj
         m = m_new
@@ -127,11 +142,13 @@ def walk_one(q, k, v, cu_seqlens, Hq, Hkv, causal, lam, scale, item, replay=None
 
 
 def prefill_fwd(q, k, v, cu_seqlens, Hq: int, Hkv: int, causal: bool = True, lam: float = 0.01,
-                scale: float | None = None, items=None, replay_bitmap=None) -> Result:
+                scale: float | None = None, items=None, replay_bitmap=None,
+                cu_seqlens_k=None) -> Result:
     """Tile walk over ``items`` (all query tiles by default).
 
-    q, k, v: float64 values ``[T, H, d]``. ``replay_bitmap``: uint32 words in
-    the interface layout; when given, decisions come from it (mask replay).
+    q, k, v: float64 values ``[T, H, d]`` (k, v over the key tokens when
+    ``cu_seqlens_k`` is given). ``replay_bitmap``: uint32 words in the
+    interface layout; when given, decisions come from it (mask replay).
     """
     if not (lam == 0 or 0 < lam < 1):
         raise ValueError("lambda must be 0 or in (0, 1)")
@@ -139,21 +156,23 @@ def prefill_fwd(q, k, v, cu_seqlens, Hq: int, Hkv: int, causal: bool = True, lam
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     cu = np.asarray(cu_seqlens, np.int64)
+    cuk = cu if cu_seqlens_k is None else np.asarray(cu_seqlens_k, np.int64)
     out = np.full((T, Hq, d), np.nan)
     lse = np.full((Hq, T), np.nan)
-    bitmap = np.zeros(layout.total_words(cu, Hq), np.uint32)
+    bitmap = np.zeros(layout.total_words(cu, Hq, cuk), np.uint32)
     margins, kept_all = {}, {}
     for item in (all_items(cu, Hq) if items is None else items):
         s, h, i = item
         replay = None
         if replay_bitmap is not None:
-            replay = layout.row_bits(replay_bitmap, cu, Hq, s, h, i)
-        o, ls, bits, mg, kept = walk_one(q, k, v, cu, Hq, Hkv, causal, lam, scale, item, replay)
+            replay = layout.row_bits(replay_bitmap, cu, Hq, s, h, i, cuk)
+        o, ls, bits, mg, kept = walk_one(q, k, v, cu, Hq, Hkv, causal, lam, scale, item, replay,
+                                         cu_seqlens_k=cuk)
         a, L = int(cu[s]), int(cu[s + 1] - cu[s])
         r0, r1 = i * TILE, min((i + 1) * TILE, L)
         out[a + r0:a + r1, h, :] = o
         lse[h, a + r0:a + r1] = ls
-        base = layout.row_offset(cu, Hq, s, h, i)
+        base = layout.row_offset(cu, Hq, s, h, i, cuk)
         for j in np.nonzero(bits)[0]:
             bitmap[base + j // 32] |= np.uint32(1 << (int(j) % 32))
         margins[item] = mg
