@@ -174,17 +174,33 @@ def item_dense_flops(i, d=128):
     return 4.0 * d * float(rows.sum())
 
 
-def oracle_baseline(problem, budget_s: float = 12.0, cores=None, seed: int = 0):
-    """Time the oracle on a bounded, deterministic sample of query tiles.
+class SavedLayer:
+    """The layer's bf16 arrays saved once under a temporary directory, so
+    oracle worker processes can memory-map them."""
 
-    Returns (dense-equivalent TFLOP/s over the sample, cores, description).
+    def __init__(self, problem):
+        self.problem = problem
+        self.dir = tempfile.mkdtemp(prefix="bsa_oracle_")
+        for name in ("q", "k", "v"):
+            np.save(os.path.join(self.dir, f"{name}.npy"), getattr(problem, name))
+
+    def close(self):
+        for name in ("q", "k", "v"):
+            os.unlink(os.path.join(self.dir, f"{name}.npy"))
+        os.rmdir(self.dir)
+
+
+def oracle_baseline(problem, budget_s: float = 12.0, cores=None, seed: int = 0, saved=None):
+    """Time the oracle on a bounded, random sample of query tiles.
+
+    Returns (dense-equivalent TFLOP/s over the sample, cores, description,
+    wall seconds, number of tiles).
     """
     import multiprocessing as mp
     cores = cores or len(os.sched_getaffinity(0))
-    tmp = tempfile.mkdtemp(prefix="bsa_oracle_")
-    np.save(os.path.join(tmp, "q.npy"), problem.q)
-    np.save(os.path.join(tmp, "k.npy"), problem.k)
-    np.save(os.path.join(tmp, "v.npy"), problem.v)
+    own = saved is None
+    saved = saved or SavedLayer(problem)
+    tmp = saved.dir
     n = (int(problem.seqlens[0]) + TILE - 1) // TILE
     rng = np.random.default_rng(seed)
     env_keep = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
@@ -213,9 +229,8 @@ def oracle_baseline(problem, budget_s: float = 12.0, cores=None, seed: int = 0):
                 os.environ.pop(k, None)
             else:
                 os.environ[k] = val
-        for f in ("q.npy", "k.npy", "v.npy"):
-            os.unlink(os.path.join(tmp, f))
-        os.rmdir(tmp)
+        if own:
+            saved.close()
     flops = sum(item_dense_flops(it[3][2]) for it in items)
     desc = (f"{len(items)} random query tiles (all key tiles up to the diagonal) of the layer, "
             f"{total} tile visits, {cores} worker processes x 1 thread, fp64")
@@ -308,6 +323,44 @@ def gpu_arm(args, rank, world, local_rank):
                           "executed_tflops": round(executed_flops(seqlens, Hq, sk, d) / m / 1e9, 1),
                           "skip_fraction": round(sk / ctiles, 5)})
 
+    # FP8 E4M3 variant of the same layer (C4): per-head quantisation by the
+    # library, then the FP8 forward; its tensor peak is the measured bf16
+    # peak times the nominal FP8/bf16 ratio of 2
+    fp8 = None
+    if not args.no_fp8:
+        codes = [torch.empty(x.shape, dtype=torch.uint8, device=dev) for x in (q, k, v)]
+        scales = [torch.empty((x.shape[1],), dtype=torch.float32, device=dev) for x in (q, k, v)]
+        for x, c8, sc in zip((q, k, v), codes, scales):
+            bsa.check(bsa.quantize_fp8(x, T, x.shape[1], d, c8, sc, stream), "quantize_fp8")
+        bsa.check(bsa.set_fp8_scales(*scales), "set_fp8_scales")
+
+        def step8(lam=args.lam):
+            st = bsa.prefill_fwd(codes[0], codes[1], codes[2], cu, p.n_seqs, Hq, Hkv, d, 1, lam,
+                                 bsa.BSA_FP8_E4M3, out, lse, bm, stream)
+            if st != 0:
+                raise bsa.BsaError(st, "bsa_prefill_fwd fp8")
+        for _ in range(3):
+            step8()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n8 = max(2, args.steps // 2)
+        ev0.record(stream)
+        for _ in range(n8):
+            step8()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        m8 = ev0.elapsed_time(ev1) / n8
+        sk8 = popcount(bm.cpu().numpy())
+        x8 = executed_flops(seqlens, Hq, sk8, d)
+        fp8 = {"workload": "the same layer in FP8 E4M3 (per-head absmax scales), bf16 output",
+               "lambda": args.lam, "ms": round(m8, 3), "dense_equiv_tflops": round(dflops / m8 / 1e9, 1),
+               "executed_tflops": round(x8 / m8 / 1e9, 1), "skip_fraction": round(sk8 / ctiles, 5),
+               "roofline_frac": round(x8 / m8 / 1e9 / (2 * peak), 4),
+               "peak": 2 * peak, "peak_source": "measured bf16 burst x nominal FP8/bf16 ratio 2"}
+        bsa.check(bsa.set_fp8_scales(None, None, None), "clear scales")
+        bsa.check(bsa.get_device_status(stream), "device status")
+        del codes, scales
+
     # dense causal attention from the box's library (torch SDPA) on the same
     # shape: the comparison for the lambda = 0 path
     dense_ref = None
@@ -396,6 +449,7 @@ def gpu_arm(args, rank, world, local_rank):
         "dense_equiv_tflop_per_step": round(dflops / 1e12, 3),
         "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
         "gpu_launches": 2 * args.steps, "lambda_sweep": sweep, "dense_reference": dense_ref,
+        "fp8": fp8,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -411,16 +465,22 @@ def reference_arm(args, rank, world):
     from gen import inputs as gi
     p = gi.config(args.config, seed=args.seed, lam=args.lam)
     vals = []
-    for _ in range(args.warmup):
-        oracle_baseline(p, budget_s=2.0)
-    for _ in range(args.steps):
-        tf, cores, desc, wall, nitems = oracle_baseline(p, budget_s=args.ref_budget)
-        vals.append((tf, wall))
+    saved = SavedLayer(p)
+    try:
+        for w in range(args.warmup):
+            oracle_baseline(p, budget_s=2.0, saved=saved, seed=1000 + w)
+        for k in range(args.steps):
+            tf, cores, desc, wall, nitems = oracle_baseline(p, budget_s=args.ref_budget, saved=saved,
+                                                            seed=k)
+            vals.append((tf, wall))
+    finally:
+        saved.close()
     tf = statistics.median(v[0] for v in vals)
     dflops = dense_flops([int(x) for x in p.seqlens], p.Hq, p.d)
     ms = dflops / (tf * 1e12) * 1e3
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(tf, 6), "unit": "TFLOP/s", "n_gpus": 0,
+        "impl": "reference", "metric": METRIC, "value": round(tf, 6), "unit": "TFLOP/s",
+        "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded generator)",
@@ -446,6 +506,7 @@ def main(argv=None):
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds per reference step")
     args = ap.parse_args(argv)

@@ -253,6 +253,32 @@ __device__ __forceinline__ void row_max64(float (&a)[8], const uint32_t (&v0)[32
   }
 }
 
+// 2^x on the FMA pipe, used for part of the exponentials so that they do not
+// all queue on the MUFU unit. Cody-Waite reduction to the nearest integer n
+// (adding and subtracting 1.5 * 2^23), a degree-3 polynomial for 2^f on
+// [-1/2, 1/2] minimising the relative error (Remez exchange, coefficients
+// from fit_exp2_poly.py; at most 7.5e-5 relative error on [-125, 8]), and
+// n added to the exponent field. Arguments are clamped at -126, where the
+// result is a non-negative denormal below 2^-125.
+constexpr float kExp2C0 = 0.9999280571937561f, kExp2C1 = 0.6932609677314758f,
+                kExp2C2 = 0.2426111251115799f, kExp2C3 = 0.0551716685295105f;
+
+__device__ __forceinline__ float exp2_fma(float x) {
+  x = fmaxf(x, -126.f);
+  const float t = __fadd_rn(x, 12582912.f);
+  const float f = __fsub_rn(x, __fsub_rn(t, 12582912.f));
+  float p = fmaf(kExp2C3, f, kExp2C2);
+  p = fmaf(p, f, kExp2C1);
+  p = fmaf(p, f, kExp2C0);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+
+// One in kFmaExpEvery exponentials of a row goes to exp2_fma (0: none).
+#ifndef BSA_FMA_EXP_EVERY
+#define BSA_FMA_EXP_EVERY 0
+#endif
+constexpr int kFmaExpEvery = BSA_FMA_EXP_EVERY;
+
 // -inf on the masked columns of one 32-column chunk: keys past the query
 // (diagonal tile) or past the sequence end (tail tile, non-causal).
 __device__ __forceinline__ void mask_chunk(uint32_t (&v)[32], int ch, bool diag, bool tailt,
@@ -571,7 +597,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
               float pe[32];
 #pragma unroll
               for (int e = 0; e < 32; ++e) {
-                pe[e] = valid ? ex2_approx(fmaf(__uint_as_float(v[e]), c, nm)) : 0.f;
+                const float xe = fmaf(__uint_as_float(v[e]), c, nm);
+                const bool on_fma = kFmaExpEvery > 0 && (e % (kFmaExpEvery > 0 ? kFmaExpEvery : 1)) ==
+                                                            (kFmaExpEvery > 0 ? kFmaExpEvery - 1 : 0);
+                pe[e] = valid ? (on_fma ? exp2_fma(xe) : ex2_approx(xe)) : 0.f;
                 sum += pe[e];
               }
               if (FP8) {
