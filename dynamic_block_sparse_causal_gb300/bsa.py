@@ -41,6 +41,12 @@ def lib() -> ctypes.CDLL:
     vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
     L.bsa_prefill_fwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp, vp]
     L.bsa_prefill_fwd.restype = i32
+    L.bsa_prefill_fwd_chunked.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
+                                          vp, vp, vp, vp]
+    L.bsa_prefill_fwd_chunked.restype = i32
+    L.bsa_skip_bitmap_words_chunked.argtypes = [ctypes.POINTER(ctypes.c_int32),
+                                                ctypes.POINTER(ctypes.c_int32), i32, i32]
+    L.bsa_skip_bitmap_words_chunked.restype = i64
     L.bsa_prefill_fwd_noalloc.argtypes = L.bsa_prefill_fwd.argtypes
     L.bsa_prefill_fwd_noalloc.restype = i32
     L.bsa_set_fp8_scales.argtypes = [vp, vp, vp]
@@ -87,6 +93,15 @@ def prefill_fwd(q, k, v, cu_seqlens, n_seqs, Hq, Hkv, d, causal, lam, dtype, out
                                  _ptr(out), _ptr(lse), _ptr(skip_bitmap), _stream(stream))
 
 
+def prefill_fwd_chunked(q, k, v, cu_seqlens_q, cu_seqlens_k, n_seqs, Hq, Hkv, d, causal, lam,
+                        dtype, out, lse, skip_bitmap, stream=None) -> int:
+    """bsa_prefill_fwd_chunked: queries are the last positions of their sequence."""
+    return lib().bsa_prefill_fwd_chunked(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q),
+                                         _ptr(cu_seqlens_k), int(n_seqs), int(Hq), int(Hkv),
+                                         int(d), int(causal), float(lam), int(dtype), _ptr(out),
+                                         _ptr(lse), _ptr(skip_bitmap), _stream(stream))
+
+
 def prefill_fwd_noalloc(q, k, v, cu_seqlens, n_seqs, Hq, Hkv, d, causal, lam, dtype, out, lse,
                         skip_bitmap, stream=None) -> int:
     """bsa_prefill_fwd_noalloc: same call, scratch from a fixed array in the
@@ -111,6 +126,17 @@ def skip_bitmap_words(cu_seqlens_host, Hq) -> int:
     cu = np.ascontiguousarray(cu_seqlens_host, dtype=np.int32)
     return lib().bsa_skip_bitmap_words(cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                                        int(cu.shape[0] - 1), int(Hq))
+
+
+def skip_bitmap_words_chunked(cu_seqlens_q_host, cu_seqlens_k_host, Hq) -> int:
+    import numpy as np
+    cq = np.ascontiguousarray(cu_seqlens_q_host, dtype=np.int32)
+    ck = np.ascontiguousarray(cu_seqlens_k_host, dtype=np.int32)
+    if cq.shape != ck.shape:
+        return -1
+    P = ctypes.POINTER(ctypes.c_int32)
+    return lib().bsa_skip_bitmap_words_chunked(cq.ctypes.data_as(P), ck.ctypes.data_as(P),
+                                               int(cq.shape[0] - 1), int(Hq))
 
 
 def get_device_status(stream=None) -> int:

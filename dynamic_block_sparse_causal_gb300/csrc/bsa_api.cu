@@ -118,17 +118,18 @@ void current_fp8_scales(const float **q, const float **k, const float **v) {
 }
 }  // namespace bsa
 
-extern "C" {
+namespace {
 
-bsa_status_t bsa_prefill_fwd(const void *q, const void *k, const void *v,
-                             const int32_t *cu_seqlens, int32_t n_seqs, int32_t Hq, int32_t Hkv,
-                             int32_t d, int32_t causal, float lambda, bsa_dtype_t dtype,
-                             void *out, float *lse, uint32_t *skip_bitmap,
-                             bsa_stream_t stream_) {
+// Shared body of bsa_prefill_fwd (cu_k == cu_q) and bsa_prefill_fwd_chunked.
+bsa_status_t prefill(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                     const int32_t *cu_seqlens_k, int32_t n_seqs, int32_t Hq, int32_t Hkv,
+                     int32_t d, int32_t causal, float lambda, bsa_dtype_t dtype, void *out,
+                     float *lse, uint32_t *skip_bitmap, bsa_stream_t stream_) {
   // ---- host-only checks: nothing is enqueued on failure
-  if (!q || !k || !v || !cu_seqlens || !out) return BSA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !cu_seqlens || !cu_seqlens_k || !out) return BSA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
-      !aligned(cu_seqlens, 4) || !aligned(lse, 4) || !aligned(skip_bitmap, 4))
+      !aligned(cu_seqlens, 4) || !aligned(cu_seqlens_k, 4) || !aligned(lse, 4) ||
+      !aligned(skip_bitmap, 4))
     return BSA_ERR_INVALID_ARG;
   if (n_seqs < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Hq > 65535) return BSA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return BSA_ERR_INVALID_ARG;
@@ -156,7 +157,8 @@ bsa_status_t bsa_prefill_fwd(const void *q, const void *k, const void *v,
   const WorkspaceLayout layout = WorkspaceLayout::make(n_seqs);
   Workspace *ws = nullptr;
   if ((st = scratch_for(dev, stream, layout.bytes, &ws)) != BSA_OK) return st;
-  if (bsa::launch_prologue(cu_seqlens, n_seqs, Hq, Hkv, ws, layout, tmpl, stream) != cudaSuccess)
+  if (bsa::launch_prologue(cu_seqlens, cu_seqlens_k, n_seqs, Hq, Hkv, causal, ws, layout, tmpl,
+                           stream) != cudaSuccess)
     return BSA_ERR_CUDA;
 
   char *base = reinterpret_cast<char *>(ws);
@@ -166,6 +168,7 @@ bsa_status_t bsa_prefill_fwd(const void *q, const void *k, const void *v,
   p.seq_bitmap_off = reinterpret_cast<const int64_t *>(base + layout.seq_bitmap_off);
   p.level_start = reinterpret_cast<const int32_t *>(base + layout.level_start);
   p.cu_seqlens = cu_seqlens;
+  p.cu_seqlens_k = cu_seqlens_k;
   p.out = out;
   p.lse = lse;
   p.bitmap = skip_bitmap;
@@ -183,6 +186,28 @@ bsa_status_t bsa_prefill_fwd(const void *q, const void *k, const void *v,
   p.debug_drop_k_load = t_drop_k_load;
   if (bsa::launch_forward(p, fp8, info->sm_count, stream) != cudaSuccess) return BSA_ERR_CUDA;
   return BSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+bsa_status_t bsa_prefill_fwd(const void *q, const void *k, const void *v,
+                             const int32_t *cu_seqlens, int32_t n_seqs, int32_t Hq, int32_t Hkv,
+                             int32_t d, int32_t causal, float lambda, bsa_dtype_t dtype,
+                             void *out, float *lse, uint32_t *skip_bitmap,
+                             bsa_stream_t stream) {
+  return prefill(q, k, v, cu_seqlens, cu_seqlens, n_seqs, Hq, Hkv, d, causal, lambda, dtype, out,
+                 lse, skip_bitmap, stream);
+}
+
+bsa_status_t bsa_prefill_fwd_chunked(const void *q, const void *k, const void *v,
+                                     const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                     int32_t n_seqs, int32_t Hq, int32_t Hkv, int32_t d,
+                                     int32_t causal, float lambda, bsa_dtype_t dtype, void *out,
+                                     float *lse, uint32_t *skip_bitmap, bsa_stream_t stream) {
+  return prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, n_seqs, Hq, Hkv, d, causal, lambda, dtype,
+                 out, lse, skip_bitmap, stream);
 }
 
 bsa_status_t bsa_set_fp8_scales(const float *q_scale, const float *k_scale,
@@ -216,6 +241,19 @@ int64_t bsa_skip_bitmap_words(const int32_t *cu, int32_t n_seqs, int32_t Hq) {
     if (L < 0) return -1;
     const int64_t n = (L + bsa::kTile - 1) / bsa::kTile;
     words += (int64_t)Hq * n * ((n + 31) / 32);
+  }
+  return words;
+}
+
+int64_t bsa_skip_bitmap_words_chunked(const int32_t *cu_q, const int32_t *cu_k, int32_t n_seqs,
+                                      int32_t Hq) {
+  if (!cu_q || !cu_k || n_seqs < 1 || Hq < 1 || cu_q[0] != 0 || cu_k[0] != 0) return -1;
+  int64_t words = 0;
+  for (int32_t s = 0; s < n_seqs; ++s) {
+    const int64_t Lq = (int64_t)cu_q[s + 1] - cu_q[s], Lk = (int64_t)cu_k[s + 1] - cu_k[s];
+    if (Lq < 0 || Lk < 0) return -1;
+    const int64_t nq = (Lq + bsa::kTile - 1) / bsa::kTile, nk = (Lk + bsa::kTile - 1) / bsa::kTile;
+    words += (int64_t)Hq * nq * ((nk + 31) / 32);
   }
   return words;
 }

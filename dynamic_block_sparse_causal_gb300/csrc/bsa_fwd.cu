@@ -50,22 +50,29 @@ namespace bsa {
 
 // ============================================================ prologue
 
+// Query-tile count of sequence s (tiles of its queries) and key-tile count.
+__device__ __forceinline__ int q_tiles(const int32_t *cu, int s) {
+  return (cu[s + 1] - cu[s] + kTile - 1) / kTile;
+}
+
 __global__ void __launch_bounds__(1024)
-prologue_kernel(const int32_t *__restrict__ cu, int n_seqs, int Hq, int Hkv, Workspace *ws,
-                int32_t *seq_sorted, int64_t *seq_bitmap_off, int32_t *level_start,
+prologue_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ cuk, int n_seqs,
+                int Hq, int Hkv, int causal, Workspace *ws, int32_t *seq_sorted,
+                int64_t *seq_bitmap_off, int32_t *level_start,
                 const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv) {
   __shared__ int s_bad, s_maxn;
   const int tid = threadIdx.x;
   if (tid == 0) {
-    s_bad = (cu[0] != 0);
+    s_bad = (cu[0] != 0) || (cuk[0] != 0);
     s_maxn = 0;
   }
   __syncthreads();
   for (int s = tid; s < n_seqs; s += blockDim.x) {
-    const int L = cu[s + 1] - cu[s];
-    if (L < 0) atomicOr(&s_bad, 1);
-    atomicMax(&s_maxn, (L + kTile - 1) / kTile);
+    const int Lq = cu[s + 1] - cu[s], Lk = cuk[s + 1] - cuk[s];
+    // queries are the last Lq positions of a sequence of Lk keys
+    if (Lq < 0 || Lk < 0 || (causal && Lk < Lq) || (Lq > 0 && Lk == 0)) atomicOr(&s_bad, 1);
+    atomicMax(&s_maxn, (Lq + kTile - 1) / kTile);
   }
   __syncthreads();
   const int maxn = s_maxn;
@@ -73,12 +80,12 @@ prologue_kernel(const int32_t *__restrict__ cu, int n_seqs, int Hq, int Hkv, Wor
   const long long U = (long long)Hkv * ((group + 1) / 2);  // work items per (sequence, tile)
   bool bad = s_bad || maxn > kMaxLevels;
   if (!bad) {
-    // longest first, ties by sequence index
+    // longest first (query tiles), ties by sequence index
     for (int s = tid; s < n_seqs; s += blockDim.x) {
-      const int ns = (cu[s + 1] - cu[s] + kTile - 1) / kTile;
+      const int ns = q_tiles(cu, s);
       int rank = 0;
       for (int t = 0; t < n_seqs; ++t) {
-        const int nt = (cu[t + 1] - cu[t] + kTile - 1) / kTile;
+        const int nt = q_tiles(cu, t);
         rank += (nt > ns) || (nt == ns && t < s);
       }
       seq_sorted[rank] = s;
@@ -87,10 +94,7 @@ prologue_kernel(const int32_t *__restrict__ cu, int n_seqs, int Hq, int Hkv, Wor
     // deepest level (longest causal rows) down to level 0.
     for (int i = tid; i < maxn; i += blockDim.x) {
       long long acc = 0;
-      for (int t = 0; t < n_seqs; ++t) {
-        const int nt = (cu[t + 1] - cu[t] + kTile - 1) / kTile;
-        acc += max(0, nt - 1 - i);
-      }
+      for (int t = 0; t < n_seqs; ++t) acc += max(0, q_tiles(cu, t) - 1 - i);
       level_start[i] = (int32_t)min(U * acc, (long long)INT_MAX);
     }
   }
@@ -98,10 +102,10 @@ prologue_kernel(const int32_t *__restrict__ cu, int n_seqs, int Hq, int Hkv, Wor
   if (tid == 0) {
     long long items = 0, words = 0;
     for (int s = 0; s < n_seqs && !bad; ++s) {
-      const int ns = (cu[s + 1] - cu[s] + kTile - 1) / kTile;
+      const int nq = q_tiles(cu, s), nk = q_tiles(cuk, s);
       seq_bitmap_off[s] = words;
-      words += (long long)Hq * ns * ((ns + 31) / 32);
-      items += U * ns;
+      words += (long long)Hq * nq * ((nk + 31) / 32);
+      items += U * nq;
     }
     if (items > INT_MAX) bad = true;
     ws->counter = 0;
@@ -117,7 +121,8 @@ prologue_kernel(const int32_t *__restrict__ cu, int n_seqs, int Hq, int Hkv, Wor
     uint64_t *d64 = reinterpret_cast<uint64_t *>(dst);
 #pragma unroll
     for (int w = 0; w < 16; ++w) d64[w] = s64[w];
-    const int T = max(cu[n_seqs], 1);
+    // token extent: query tokens for the Q map, key tokens for K and V
+    const int T = max(tid == 0 ? cu[n_seqs] : cuk[n_seqs], 1);
     asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 2, %1;" ::"l"(dst),
                  "r"(T)
                  : "memory");
@@ -125,12 +130,14 @@ prologue_kernel(const int32_t *__restrict__ cu, int n_seqs, int Hq, int Hkv, Wor
   }
 }
 
-cudaError_t launch_prologue(const int32_t *cu_seqlens, int n_seqs, int Hq, int Hkv, Workspace *ws,
+cudaError_t launch_prologue(const int32_t *cu_seqlens, const int32_t *cu_seqlens_k, int n_seqs,
+                            int Hq, int Hkv, int causal, Workspace *ws,
                             const WorkspaceLayout &layout, const CUtensorMap tmpl[3],
                             cudaStream_t stream) {
   char *base = reinterpret_cast<char *>(ws);
   prologue_kernel<<<1, 1024, 0, stream>>>(
-      cu_seqlens, n_seqs, Hq, Hkv, ws, reinterpret_cast<int32_t *>(base + layout.seq_sorted),
+      cu_seqlens, cu_seqlens_k, n_seqs, Hq, Hkv, causal, ws,
+      reinterpret_cast<int32_t *>(base + layout.seq_sorted),
       reinterpret_cast<int64_t *>(base + layout.seq_bitmap_off),
       reinterpret_cast<int32_t *>(base + layout.level_start), tmpl[0], tmpl[1], tmpl[2]);
   return cudaGetLastError();
@@ -228,7 +235,7 @@ __device__ void fetch_item(const FwdParams &p, int total_items, int maxn, int *d
   const int pidx = r % U;
   const int kvh = pidx / p.pairs_per_group, pp = pidx % p.pairs_per_group;
   const int h0 = kvh * p.group + 2 * pp;
-  const int a = p.cu_seqlens[s];
+  const int a = p.cu_seqlens[s], ak = p.cu_seqlens_k[s];
   dst[0] = 1;
   dst[1] = s;
   dst[2] = kvh;
@@ -237,6 +244,8 @@ __device__ void fetch_item(const FwdParams &p, int total_items, int maxn, int *d
   dst[5] = lo;
   dst[6] = a;
   dst[7] = p.cu_seqlens[s + 1] - a;
+  dst[8] = ak;
+  dst[9] = p.cu_seqlens_k[s + 1] - ak;
 }
 
 // Running row max over two 32-register chunks (three-input max, eight
@@ -273,6 +282,17 @@ __device__ __forceinline__ float exp2_fma(float x) {
   return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
 }
 
+// Polling budget of the pipeline waits before they start to suspend: the
+// single-thread MMA issuer / TMA producer, and the softmax warpgroups.
+#ifndef BSA_SPIN_ISSUER
+#define BSA_SPIN_ISSUER 0
+#endif
+#ifndef BSA_SPIN_SOFTMAX
+#define BSA_SPIN_SOFTMAX 0
+#endif
+constexpr int kSpinIssuer = BSA_SPIN_ISSUER;
+constexpr int kSpinSoftmax = BSA_SPIN_SOFTMAX;
+
 // One in kFmaExpEvery exponentials of a row goes to exp2_fma (0: none).
 #ifndef BSA_FMA_EXP_EVERY
 #define BSA_FMA_EXP_EVERY 0
@@ -280,13 +300,15 @@ __device__ __forceinline__ float exp2_fma(float x) {
 constexpr int kFmaExpEvery = BSA_FMA_EXP_EVERY;
 
 // -inf on the masked columns of one 32-column chunk: keys past the query
-// (diagonal tile) or past the sequence end (tail tile, non-causal).
+// (row r of the query tile sees columns up to r + doff of this key tile) or
+// past the end of the keys (tail tile, non-causal).
 __device__ __forceinline__ void mask_chunk(uint32_t (&v)[32], int ch, bool diag, bool tailt,
-                                           int row, int key0, int L) {
+                                           int row, int doff, int key0, int Lk) {
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
     const int col = ch * 32 + e;
-    if ((diag && col > row) || (tailt && key0 + col >= L)) v[e] = __float_as_uint(-INFINITY);
+    if ((diag && col > row + doff) || (tailt && key0 + col >= Lk))
+      v[e] = __float_as_uint(-INFINITY);
   }
 }
 
@@ -298,7 +320,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar[B_COUNT];
   __shared__ uint32_t tmem_sh;
-  __shared__ int item_sh[2][8];
+  __shared__ int item_sh[2][10];
   __shared__ volatile int vote_sh[2];
   __shared__ volatile int abort_sh;
 
@@ -341,8 +363,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     const int *I = item_sh[it & 1];
     if (!I[0] || abort_sh) break;
     const int s = I[1], kvh = I[2], h0 = I[3], h1 = I[4], qi = I[5], a = I[6], L = I[7];
-    const int n = (L + kTile - 1) / kTile;
-    const int last = p.causal ? qi : n - 1;
+    const int ak = I[8], Lk = I[9];
+    // queries are the last L of Lk positions: query row r sits at key position off + r
+    const int off = Lk - L;
+    const int nq = (L + kTile - 1) / kTile, nk = (Lk + kTile - 1) / kTile;
+    const int qlast = min(qi * kTile + kTile, L) - 1;   // last valid row of the query tile
+    const int last = p.causal ? min((off + qlast) / kTile, nk - 1) : nk - 1;
     const bool has1 = h1 >= 0;
     bool ok = true;
 
@@ -360,24 +386,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         qc_last = (int)qc++;
         for (int j = 0; j <= last && ok; ++j) {
           const uint32_t st = kc % kKStages;
-          ok = mbar_wait(&bar[B_KE + st], ((kc / kKStages) & 1) ^ 1, limit);
+          ok = mbar_wait(&bar[B_KE + st], ((kc / kKStages) & 1) ^ 1, limit, kSpinIssuer);
           if (!ok) break;
           if ((int)kc != p.debug_drop_k_load) {
             mbar_expect_tx(&bar[B_KF + st], C::kTileBytes);
             for (int b = 0; b < C::kBoxes; ++b)
               tma_load_3d(sptr + SM_K + st * kRegion + b * kBox, tk, &bar[B_KF + st],
-                          b * C::kBoxCols, kvh, a + j * kTile);
+                          b * C::kBoxCols, kvh, ak + j * kTile);
             kc_last[st] = (int)kc;
           }
           ++kc;
           if (v_prefetch) {
             const uint32_t vs = vc % kVStages;
-            ok = mbar_wait(&bar[B_VE + vs], ((vc / kVStages) & 1) ^ 1, limit);
+            ok = mbar_wait(&bar[B_VE + vs], ((vc / kVStages) & 1) ^ 1, limit, kSpinIssuer);
             if (!ok) break;
             mbar_expect_tx(&bar[B_VF + vs], C::kTileBytes);
             for (int b = 0; b < C::kBoxes; ++b)
               tma_load_3d(sptr + SM_V + vs * kRegion + b * kBox, tv, &bar[B_VF + vs],
-                          b * C::kBoxCols, kvh, a + j * kTile);
+                          b * C::kBoxCols, kvh, ak + j * kTile);
             vc_last[vs] = (int)vc;
             ++vc;
           }
@@ -393,22 +419,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         // V_j request from this thread (skipping on): only kept tiles are loaded
         auto issue_v = [&](int j) -> bool {
           const uint32_t vs = vc % kVStages;
-          if (!mbar_wait(&bar[B_VE + vs], ((vc / kVStages) & 1) ^ 1, limit)) return false;
+          if (!mbar_wait(&bar[B_VE + vs], ((vc / kVStages) & 1) ^ 1, limit, kSpinIssuer)) return false;
           mbar_expect_tx(&bar[B_VF + vs], C::kTileBytes);
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_3d(sptr + SM_V + vs * kRegion + b * kBox, tv, &bar[B_VF + vs],
-                        b * C::kBoxCols, kvh, a + j * kTile);
+                        b * C::kBoxCols, kvh, ak + j * kTile);
           vc_last[vs] = (int)vc;
           return true;
         };
         do {
           // key tile 0 is never skipped: request its V before anything else
           if (!v_prefetch && !(ok = issue_v(0))) break;
-          ok = mbar_wait(&bar[B_Q], qc & 1, limit);
+          ok = mbar_wait(&bar[B_Q], qc & 1, limit, kSpinIssuer);
           ++qc;
           if (!ok) break;
           uint32_t st = kc % kKStages;
-          ok = mbar_wait(&bar[B_KF + st], (kc / kKStages) & 1, limit);
+          ok = mbar_wait(&bar[B_KF + st], (kc / kKStages) & 1, limit, kSpinIssuer);
           if (!ok) break;
           tc_fence_after();
           uint32_t ks = sbase + SM_K + st * kRegion;
@@ -427,20 +453,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             const uint32_t vs = vc % kVStages;
             auto wait_v = [&]() -> bool {
               if (vready) return true;
-              if (!mbar_wait(&bar[B_VF + vs], (vc / kVStages) & 1, limit)) return false;
+              if (!mbar_wait(&bar[B_VF + vs], (vc / kVStages) & 1, limit, kSpinIssuer)) return false;
               tc_fence_after();
               vready = true;
               return true;
             };
             // ---- slot 0: vote, then P.V (if kept) before the next S overwrites P
-            ok = mbar_wait(&bar[B_VOTE + 0], vt0 & 1, limit);
+            ok = mbar_wait(&bar[B_VOTE + 0], vt0 & 1, limit, kSpinIssuer);
             ++vt0;
             if (!ok) break;
             const bool keep0 = vote_sh[0] == 0;
             if (keep0) {
               if (!vload && !(ok = issue_v(j))) break;
               vload = true;
-              ok = mbar_wait(&bar[B_PRDY + 0], pr0 & 1, limit);
+              ok = mbar_wait(&bar[B_PRDY + 0], pr0 & 1, limit, kSpinIssuer);
               ++pr0;
               if (!ok || !(ok = wait_v())) break;
               tc_fence_after();
@@ -450,7 +476,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             }
             if (j < last) {
               st = kc % kKStages;
-              ok = mbar_wait(&bar[B_KF + st], (kc / kKStages) & 1, limit);
+              ok = mbar_wait(&bar[B_KF + st], (kc / kKStages) & 1, limit, kSpinIssuer);
               if (!ok) break;
               tc_fence_after();
               ks = sbase + SM_K + st * kRegion;
@@ -459,14 +485,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             }
             // ---- slot 1
             if (has1) {
-              ok = mbar_wait(&bar[B_VOTE + 1], vt1 & 1, limit);
+              ok = mbar_wait(&bar[B_VOTE + 1], vt1 & 1, limit, kSpinIssuer);
               ++vt1;
               if (!ok) break;
               const bool keep1 = vote_sh[1] == 0;
               if (keep1) {
                 if (!vload && !(ok = issue_v(j))) break;
                 vload = true;
-                ok = mbar_wait(&bar[B_PRDY + 1], pr1 & 1, limit);
+                ok = mbar_wait(&bar[B_PRDY + 1], pr1 & 1, limit, kSpinIssuer);
                 ++pr1;
                 if (!ok || !(ok = wait_v())) break;
                 tc_fence_after();
@@ -505,21 +531,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         const uint32_t tO = tmem + kColO + slot * 128 + lane_off;
         const int qpos = qi * kTile + row;
         const bool valid = qpos < L;
-        const bool tail = !p.causal && (L % kTile) != 0;
+        const bool tail = !p.causal && (Lk % kTile) != 0;
         float c = p.c;
         if (FP8) c *= p.q_scale[h] * p.k_scale[kvh];
-        const int W = (n + 31) >> 5;
-        const long long boff = p.seq_bitmap_off[s] + ((long long)h * n + qi) * W;
+        const int W = (nk + 31) >> 5;
+        const long long boff = p.seq_bitmap_off[s] + ((long long)h * nq + qi) * W;
         float m2 = -INFINITY, mref = 0.f, l = 0.f;
         uint32_t word = 0;
         bool have_kept = false;
 
         for (int j = 0; j <= last; ++j) {
-          if (!mbar_wait(&bar[B_SF + slot], sc & 1, limit)) abort_sh = 1;
+          if (!mbar_wait(&bar[B_SF + slot], sc & 1, limit, kSpinSoftmax)) abort_sh = 1;
           ++sc;
           tc_fence_after();
-          const bool diag = p.causal && j == qi;
-          const bool tailt = tail && j == n - 1;
+          const int doff = off + (qi - j) * kTile;   // row r sees columns <= r + doff
+          const bool diag = p.causal && doff < kTile - 1;
+          const bool tailt = tail && j == nk - 1;
           float rm;
           {
             float acc[8];
@@ -533,8 +560,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
               tmem_wait_ld(v0);
               reg_fence(v1);
               if (diag || tailt) {
-                mask_chunk(v0, 2 * half, diag, tailt, row, j * kTile, L);
-                mask_chunk(v1, 2 * half + 1, diag, tailt, row, j * kTile, L);
+                mask_chunk(v0, 2 * half, diag, tailt, row, doff, j * kTile, Lk);
+                mask_chunk(v1, 2 * half + 1, diag, tailt, row, doff, j * kTile, Lk);
               }
               row_max64(acc, v0, v1);
             }
@@ -586,37 +613,52 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             m2 = mnew;
             // P = exp2(S c - m_ref), written over the S columns already read:
             // chunk ch (keys 32ch..32ch+31) goes to columns 16ch.. (bf16) or 8ch.. (e4m3)
-            float sum = 0.f;
             const float nm = -mref;
+            float psum[8];
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-              uint32_t v[32];
-              tmem_ld32(tS + ch * 32, v);
-              tmem_wait_ld(v);
-              if (diag || tailt) mask_chunk(v, ch, diag, tailt, row, j * kTile, L);
-              float pe[32];
+            for (int k = 0; k < 8; ++k) psum[k] = 0.f;
+            {
+              uint32_t va[32], vb[32];
+              tmem_ld32(tS, va);
+              tmem_wait_ld(va);
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const float xe = fmaf(__uint_as_float(v[e]), c, nm);
-                const bool on_fma = kFmaExpEvery > 0 && (e % (kFmaExpEvery > 0 ? kFmaExpEvery : 1)) ==
-                                                            (kFmaExpEvery > 0 ? kFmaExpEvery - 1 : 0);
-                pe[e] = valid ? (on_fma ? exp2_fma(xe) : ex2_approx(xe)) : 0.f;
-                sum += pe[e];
-              }
-              if (FP8) {
-                uint32_t w8[8];
+              for (int ch = 0; ch < 4; ++ch) {
+                uint32_t(&v)[32] = (ch & 1) ? vb : va;
+                uint32_t(&nxt)[32] = (ch & 1) ? va : vb;
+                if (ch < 3) tmem_ld32(tS + (ch + 1) * 32, nxt);   // overlaps this chunk's math
+                if (diag || tailt) mask_chunk(v, ch, diag, tailt, row, doff, j * kTile, Lk);
+                // p = exp2(s c - m_ref), packed as it is produced
+                auto pexp = [&](int e) -> float {
+                  const float xe = fmaf(__uint_as_float(v[e]), c, nm);
+                  const bool on_fma = kFmaExpEvery > 0 && (e % (kFmaExpEvery > 0 ? kFmaExpEvery : 1)) ==
+                                                              (kFmaExpEvery > 0 ? kFmaExpEvery - 1 : 0);
+                  const float pv = valid ? (on_fma ? exp2_fma(xe) : ex2_approx(xe)) : 0.f;
+                  psum[e & 7] += pv;
+                  return pv;
+                };
+                if (FP8) {
+                  uint32_t w8[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                  w8[k] = (uint32_t)pack_e4m3x2(pe[4 * k], pe[4 * k + 1]) |
-                          ((uint32_t)pack_e4m3x2(pe[4 * k + 2], pe[4 * k + 3]) << 16);
-                tmem_st8(tS + ch * 8, w8);
-              } else {
-                uint32_t w2[16];
+                  for (int k = 0; k < 8; ++k) {
+                    const float p0 = pexp(4 * k), p1 = pexp(4 * k + 1);
+                    const float p2 = pexp(4 * k + 2), p3 = pexp(4 * k + 3);
+                    w8[k] = (uint32_t)pack_e4m3x2(p0, p1) | ((uint32_t)pack_e4m3x2(p2, p3) << 16);
+                  }
+                  tmem_st8(tS + ch * 8, w8);
+                } else {
+                  uint32_t w2[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) w2[k] = pack_bf16x2(pe[2 * k], pe[2 * k + 1]);
-                tmem_st16(tS + ch * 16, w2);
+                  for (int k = 0; k < 16; ++k) {
+                    const float p0 = pexp(2 * k), p1 = pexp(2 * k + 1);
+                    w2[k] = pack_bf16x2(p0, p1);
+                  }
+                  tmem_st16(tS + ch * 16, w2);
+                }
+                if (ch < 3) tmem_wait_ld(nxt);
               }
             }
+            const float sum = ((psum[0] + psum[1]) + (psum[2] + psum[3])) +
+                              ((psum[4] + psum[5]) + (psum[6] + psum[7]));
             tmem_wait_st();
             l += sum;
             tc_fence_before();

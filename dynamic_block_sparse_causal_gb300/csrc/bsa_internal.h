@@ -27,7 +27,7 @@ struct alignas(128) Workspace {
   int32_t status;        // kStatus* bits, sticky until read by the host
   int32_t total_items;   // 0 when cu_seqlens was rejected
   int32_t max_tiles;     // longest sequence, in tiles
-  int32_t total_tokens;  // cu_seqlens[n_seqs]
+  int32_t total_tokens;  // cu_seqlens[n_seqs] (query tokens)
   int32_t pad_[27];
 };
 
@@ -52,7 +52,8 @@ struct FwdParams {
   const int32_t *seq_sorted;
   const int64_t *seq_bitmap_off;
   const int32_t *level_start;
-  const int32_t *cu_seqlens;
+  const int32_t *cu_seqlens;     // query boundaries
+  const int32_t *cu_seqlens_k;   // key/value boundaries (== cu_seqlens unless chunked)
   void *out;                 // bf16 [T, Hq, d]
   float *lse;                // [Hq, T] or null
   uint32_t *bitmap;          // or null
@@ -69,9 +70,10 @@ struct FwdParams {
 };
 
 // Host-side launchers (bsa_fwd.cu).
-cudaError_t launch_prologue(const int32_t *cu_seqlens, int n_seqs, int Hq, int Hkv,
-                            Workspace *ws, const WorkspaceLayout &layout,
-                            const CUtensorMap tmpl[3], cudaStream_t stream);
+cudaError_t launch_prologue(const int32_t *cu_seqlens, const int32_t *cu_seqlens_k, int n_seqs,
+                            int Hq, int Hkv, int causal, Workspace *ws,
+                            const WorkspaceLayout &layout, const CUtensorMap tmpl[3],
+                            cudaStream_t stream);
 cudaError_t launch_forward(const FwdParams &p, bool fp8, int num_ctas, cudaStream_t stream);
 size_t forward_smem_bytes();
 cudaError_t prepare_forward();   // per device: opt in to the shared-memory size

@@ -53,10 +53,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe of the phase (no suspension).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of the given parity to complete, giving up after
-// `limit_ns` nanoseconds of wall time. Returns false on time-out.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+// `limit_ns` nanoseconds of wall time. Returns false on time-out. The first
+// `spin` probes poll without suspending (lowest wake-up latency for a
+// thread that has nothing else to do); after that the thread suspends in
+// try_wait between probes.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                          int spin = 0) {
   const uint32_t a = smem_u32(bar);
+  for (int i = 0; i < spin; ++i)
+    if (mbar_test_wait(a, parity)) return true;
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {

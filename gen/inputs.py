@@ -56,6 +56,9 @@ class Problem:
     d: int
     causal: bool = True
     lam: float = 0.01
+    # chunked prefill: key/value boundaries when q holds only each sequence's
+    # last positions (k, v are then packed by these instead of cu_seqlens)
+    cu_seqlens_k: np.ndarray | None = None
 
     @property
     def n_seqs(self) -> int:
@@ -137,6 +140,17 @@ def packed(name: str, lengths, Hq: int, Hkv: int, seed: int = 0, d: int = HEAD_D
         a, b = int(cu[s]), int(cu[s + 1])
         q[a:b], k[a:b], v[a:b] = sequence(rng, L, Hq, Hkv, d, **recipe)
     return Problem(name, q, k, v, cu, Hq, Hkv, d, causal, lam)
+
+
+def chunk(p: Problem, lq) -> Problem:
+    """Keep only the last ``lq[s]`` queries of every sequence of ``p`` (all keys stay)."""
+    qs, cuq = [], [0]
+    for s, n in enumerate(lq):
+        b = int(p.cu_seqlens[s + 1])
+        qs.append(p.q[b - int(n):b])
+        cuq.append(cuq[-1] + int(n))
+    return Problem(p.name + "_chunk", np.concatenate(qs), p.k, p.v, np.asarray(cuq, np.int32),
+                   p.Hq, p.Hkv, p.d, p.causal, p.lam, cu_seqlens_k=p.cu_seqlens.copy())
 
 
 def varlen_lengths(seed: int = 0, n: int = 16, lo: int = 4096, hi: int = 65536) -> list:

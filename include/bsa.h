@@ -106,6 +106,37 @@ bsa_status_t bsa_prefill_fwd(const void *q, const void *k, const void *v,
                              bsa_stream_t stream);
 
 /*
+ * Chunked prefill: the same forward pass when a sequence's queries are only
+ * its last Lq positions and its keys/values (earlier chunks included, e.g.
+ * read back from a KV cache) number Lk >= Lq -- the chunked prefill that the
+ * prefill-acceleration blog (mhpq.cn news 313192, §3.1) and FlowPrefill
+ * describe for splitting long prompts. Query row r of sequence s sits at key
+ * position Lk - Lq + r (bottom-right causal alignment); key tiles are visited
+ * from 0 in order with the same skip rule.
+ *
+ * q            device [Tq, Hq, d], packed by cu_seqlens_q.
+ * k, v         device [Tk, Hkv, d], packed by cu_seqlens_k.
+ * cu_seqlens_q, cu_seqlens_k   device int32 [n_seqs + 1] prefix sums (both
+ *              start at 0); causal requires Lk >= Lq for every sequence.
+ *              Violations are recorded on the device (BSA_ERR_BAD_SEQLENS).
+ * out          device bf16 [Tq, Hq, d]; lse device float32 [Hq, Tq] or NULL.
+ * skip_bitmap  one row per query tile: n_q = ceil(Lq/128) rows of
+ *              W = ceil(ceil(Lk/128)/32) words per (sequence, head);
+ *              sequence s starts at word sum_{t<s}(Hq n_q,t W_t), row (s,h,i)
+ *              at + (h n_q + i) W; bit j = key tile j. Size:
+ *              bsa_skip_bitmap_words_chunked().
+ * Other arguments, conventions and errors as bsa_prefill_fwd, which is this
+ * call with cu_seqlens_k == cu_seqlens_q.
+ */
+bsa_status_t bsa_prefill_fwd_chunked(const void *q, const void *k, const void *v,
+                                     const int32_t *cu_seqlens_q,
+                                     const int32_t *cu_seqlens_k, int32_t n_seqs,
+                                     int32_t Hq, int32_t Hkv, int32_t d,
+                                     int32_t causal, float lambda,
+                                     bsa_dtype_t dtype, void *out, float *lse,
+                                     uint32_t *skip_bitmap, bsa_stream_t stream);
+
+/*
  * Same forward pass as bsa_prefill_fwd, same arguments and results, for
  * callers that may not allocate device memory -- for example a serving
  * engine that reserves nearly all of HBM for its own pool up front and
@@ -160,6 +191,14 @@ bsa_status_t bsa_quantize_fp8(const void *x_bf16, int64_t tokens, int32_t H,
  */
 int64_t bsa_skip_bitmap_words(const int32_t *cu_seqlens_host, int32_t n_seqs,
                               int32_t Hq);
+
+/*
+ * Skip-bitmap size in words for bsa_prefill_fwd_chunked, from HOST copies of
+ * both boundary arrays. Returns -1 if either is malformed.
+ */
+int64_t bsa_skip_bitmap_words_chunked(const int32_t *cu_seqlens_q_host,
+                                      const int32_t *cu_seqlens_k_host,
+                                      int32_t n_seqs, int32_t Hq);
 
 /*
  * Synchronises `stream`, returns the device-side status recorded by the

@@ -46,6 +46,8 @@ def run(p, lam=None, causal=None, fp8=None, stream=None, out_fill=float("nan")):
     causal = p.causal if causal is None else causal
     T = p.total_tokens
     cu = torch.from_numpy(p.cu_seqlens.astype(np.int32)).cuda()
+    chunked = p.cu_seqlens_k is not None
+    cuk = torch.from_numpy(p.cu_seqlens_k.astype(np.int32)).cuda() if chunked else None
     if fp8 is None:
         q, k, v = to_dev_bf16(p.q), to_dev_bf16(p.k), to_dev_bf16(p.v)
         dtype = b.BSA_BF16
@@ -56,10 +58,17 @@ def run(p, lam=None, causal=None, fp8=None, stream=None, out_fill=float("nan")):
         dtype = b.BSA_FP8_E4M3
     out = torch.full((T, p.Hq, p.d), out_fill, dtype=torch.bfloat16, device="cuda")
     lse = torch.full((p.Hq, T), float("nan"), dtype=torch.float32, device="cuda")
-    nw = b.skip_bitmap_words(p.cu_seqlens, p.Hq)
+    if chunked:
+        nw = b.skip_bitmap_words_chunked(p.cu_seqlens, p.cu_seqlens_k, p.Hq)
+    else:
+        nw = b.skip_bitmap_words(p.cu_seqlens, p.Hq)
     bm = torch.full((max(nw, 1),), -1, dtype=torch.int32, device="cuda")
-    st = b.prefill_fwd(q, k, v, cu, p.n_seqs, p.Hq, p.Hkv, p.d, int(causal), lam, dtype,
-                       out, lse, bm, stream)
+    if chunked:
+        st = b.prefill_fwd_chunked(q, k, v, cu, cuk, p.n_seqs, p.Hq, p.Hkv, p.d, int(causal), lam,
+                                   dtype, out, lse, bm, stream)
+    else:
+        st = b.prefill_fwd(q, k, v, cu, p.n_seqs, p.Hq, p.Hkv, p.d, int(causal), lam, dtype,
+                           out, lse, bm, stream)
     b.check(st, "bsa_prefill_fwd")
     torch.cuda.synchronize()
     b.check(b.get_device_status(stream), "device status")
@@ -94,14 +103,15 @@ def sample_items(p, max_items=None, seed=0):
     return sorted(pick)
 
 
-def _values(p, fp8, rows, heads_q, heads_kv):
-    """fp64 values of the token rows ``rows`` for the given heads."""
+def _values(p, fp8, qrows, krows, heads_q, heads_kv):
+    """fp64 values of query rows ``qrows`` and key/value rows ``krows``."""
+    rows = (qrows, krows, krows)
     if fp8 is None:
-        return (numerics.bf16_to_f64(p.q[rows][:, heads_q]), numerics.bf16_to_f64(p.k[rows][:, heads_kv]),
-                numerics.bf16_to_f64(p.v[rows][:, heads_kv]))
+        return tuple(numerics.bf16_to_f64(x[r][:, hs])
+                     for x, r, hs in zip((p.q, p.k, p.v), rows, (heads_q, heads_kv, heads_kv)))
     out = []
-    for codes, scale, hs in zip(fp8[:3], fp8[3:], (heads_q, heads_kv, heads_kv)):
-        out.append(numerics.e4m3_to_f64(codes[rows][:, hs]) * np.asarray(scale, np.float64)[hs][None, :, None])
+    for codes, scale, r, hs in zip(fp8[:3], fp8[3:], rows, (heads_q, heads_kv, heads_kv)):
+        out.append(numerics.e4m3_to_f64(codes[r][:, hs]) * np.asarray(scale, np.float64)[hs][None, :, None])
     return tuple(out)
 
 
@@ -109,6 +119,7 @@ def compare(p, g, items=None, fp8=None, check_bits=True):
     """Compare a GPU result with the oracle on ``items`` (all query tiles by
     default); return a dict of metrics, asserting the tolerances."""
     cu = p.cu_seqlens
+    cuk = p.cu_seqlens if p.cu_seqlens_k is None else p.cu_seqlens_k
     lam, causal = g["lam"], g["causal"]
     G = p.Hq // p.Hkv
     scale = 1.0 / math.sqrt(p.d)
@@ -120,14 +131,20 @@ def compare(p, g, items=None, fp8=None, check_bits=True):
     for item in (tile_walk.all_items(cu, p.Hq) if items is None else items):
         s, h, i = item
         a, L = int(cu[s]), int(cu[s + 1] - cu[s])
-        last = i if causal else layout.tiles(L) - 1
-        hi = min((last + 1) * 128, L)
-        q, k, v = _values(p, fp8, slice(a, a + hi), [h], [h // G])
-        # causal: keys past the diagonal tile are never visited, so the sequence
-        # truncated after it walks identically (non-causal visits all: hi == L)
-        sub_cu = [0, hi]
-        _, _, want, mg, _ = tile_walk.walk_one(q, k, v, sub_cu, 1, 1, causal, lam, scale, (0, 0, i))
-        row = layout.row_bits(g["bitmap"], cu, p.Hq, s, h, i)
+        ak, Lk = int(cuk[s]), int(cuk[s + 1] - cuk[s])
+        off = Lk - L
+        r0, r1 = i * 128, min(i * 128 + 128, L)
+        last = min((off + r1 - 1) // 128, layout.tiles(Lk) - 1) if causal else layout.tiles(Lk) - 1
+        hi = min((last + 1) * 128, Lk)
+        # causal: keys past the last visited tile are never read, so the
+        # sequence truncated after it (queries keep their positions, so the
+        # chunk keeps the rows that end at key hi) walks identically
+        q_hi = hi - off if causal else L
+        q, k, v = _values(p, fp8, slice(a, a + q_hi), slice(ak, ak + hi), [h], [h // G])
+        sub_q, sub_k = [0, q_hi], [0, hi]
+        _, _, want, mg, _ = tile_walk.walk_one(q, k, v, sub_q, 1, 1, causal, lam, scale, (0, 0, i),
+                                               cu_seqlens_k=sub_k)
+        row = layout.row_bits(g["bitmap"], cu, p.Hq, s, h, i, cuk)
         assert not row[last + 1:].any(), f"bit set on an unvisited tile of {item}"
         got, want = row[:last + 1], want[:last + 1]
         for j in np.nonzero(got != want)[0]:
@@ -135,9 +152,9 @@ def compare(p, g, items=None, fp8=None, check_bits=True):
                 near += 1
             else:
                 bad_bits += 1
-        o_ref, lse_ref, _, _, _ = tile_walk.walk_one(q, k, v, sub_cu, 1, 1, causal, lam, scale,
-                                                     (0, 0, i), replay=got)
-        r0, r1 = a + i * 128, a + min(i * 128 + 128, L)
+        o_ref, lse_ref, _, _, _ = tile_walk.walk_one(q, k, v, sub_q, 1, 1, causal, lam, scale,
+                                                     (0, 0, i), replay=got, cu_seqlens_k=sub_k)
+        r0, r1 = a + r0, a + r1
         o_gpu = g["out"][r0:r1, h].float().cpu().numpy().astype(np.float64)
         l_gpu = g["lse"][h, r0:r1].cpu().numpy().astype(np.float64)
         d = np.abs(o_gpu - o_ref)

@@ -91,6 +91,20 @@ def test_bitmap_words_match_layout(L, cu, Hq):
     assert L.skip_bitmap_words(np.array(cu, np.int32), Hq) == layout.total_words(cu, Hq)
 
 
+@pytest.mark.parametrize("cuq,cuk,Hq", [([0, 200], [0, 1000], 3), ([0, 10, 300], [0, 100, 5220], 2),
+                                        ([0, 2048], [0, 2048], 4), ([0, 0, 77], [0, 64, 77], 1)])
+def test_chunked_bitmap_words_match_layout(L, cuq, cuk, Hq):
+    assert L.skip_bitmap_words_chunked(np.array(cuq, np.int32), np.array(cuk, np.int32), Hq) == \
+        layout.total_words(cuq, Hq, cuk)
+
+
+def test_chunked_argument_checks(L):
+    args = (16, 32, 48, 64, 96, 1, 4, 2, 128, 1, 0.01, 0, 80, None, None)
+    assert L.prefill_fwd_chunked(*(args[:4] + (None,) + args[5:])) == 1    # no cu_seqlens_k
+    assert L.prefill_fwd_chunked(*(args[:4] + (98,) + args[5:])) == 1      # misaligned
+    assert L.prefill_fwd_chunked(*(args[:8] + (64,) + args[9:])) == 2      # d != 128
+
+
 def test_bitmap_words_rejects_bad_seqlens(L):
     assert L.skip_bitmap_words(np.array([1, 5], np.int32), 1) == -1
     assert L.skip_bitmap_words(np.array([0, 5, 3], np.int32), 1) == -1
