@@ -44,6 +44,9 @@ def lib() -> ctypes.CDLL:
     L.bsa_prefill_fwd_chunked.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
                                           vp, vp, vp, vp]
     L.bsa_prefill_fwd_chunked.restype = i32
+    L.bsa_prefill_fwd_paged.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, i32, i32, i32, i32, i32,
+                                        f32, i32, vp, vp, vp, vp]
+    L.bsa_prefill_fwd_paged.restype = i32
     L.bsa_skip_bitmap_words_chunked.argtypes = [ctypes.POINTER(ctypes.c_int32),
                                                 ctypes.POINTER(ctypes.c_int32), i32, i32]
     L.bsa_skip_bitmap_words_chunked.restype = i64
@@ -100,6 +103,17 @@ def prefill_fwd_chunked(q, k, v, cu_seqlens_q, cu_seqlens_k, n_seqs, Hq, Hkv, d,
                                          _ptr(cu_seqlens_k), int(n_seqs), int(Hq), int(Hkv),
                                          int(d), int(causal), float(lam), int(dtype), _ptr(out),
                                          _ptr(lse), _ptr(skip_bitmap), _stream(stream))
+
+
+def prefill_fwd_paged(q, k_cache, v_cache, page_table, max_pages_per_seq, num_pages, cu_seqlens_q,
+                      cu_seqlens_k, n_seqs, Hq, Hkv, d, causal, lam, dtype, out, lse, skip_bitmap,
+                      stream=None) -> int:
+    """bsa_prefill_fwd_paged: keys/values from 128-token pages via a page table."""
+    return lib().bsa_prefill_fwd_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
+                                       int(max_pages_per_seq), int(num_pages), _ptr(cu_seqlens_q),
+                                       _ptr(cu_seqlens_k), int(n_seqs), int(Hq), int(Hkv), int(d),
+                                       int(causal), float(lam), int(dtype), _ptr(out), _ptr(lse),
+                                       _ptr(skip_bitmap), _stream(stream))
 
 
 def prefill_fwd_noalloc(q, k, v, cu_seqlens, n_seqs, Hq, Hkv, d, causal, lam, dtype, out, lse,

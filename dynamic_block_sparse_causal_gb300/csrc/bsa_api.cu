@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <climits>
 #include <cmath>
 #include <cstring>
 #include <map>
@@ -92,10 +93,11 @@ bsa_status_t scratch_for(int dev, cudaStream_t stream, size_t bytes, Workspace *
 }
 
 // [tokens, H, 128] tiles of 128 rows x 128 bytes, 128-byte swizzle. The token
-// extent is a placeholder (1) that the prologue replaces with cu[n_seqs].
-bool encode_tile_map(CUtensorMap *m, const void *base, int H, bool fp8) {
+// extent is a placeholder (1) that the prologue replaces with cu[n_seqs],
+// except for a paged K/V pool, whose extent (pages x 128) is known here.
+bool encode_tile_map(CUtensorMap *m, const void *base, int H, bool fp8, uint64_t tokens = 1) {
   const cuuint64_t elem = fp8 ? 1 : 2;
-  cuuint64_t dims[3] = {(cuuint64_t)bsa::kHeadDim, (cuuint64_t)H, 1};
+  cuuint64_t dims[3] = {(cuuint64_t)bsa::kHeadDim, (cuuint64_t)H, (cuuint64_t)tokens};
   cuuint64_t strides[2] = {bsa::kHeadDim * elem, (cuuint64_t)H * bsa::kHeadDim * elem};
   cuuint32_t box[3] = {(cuuint32_t)(128 / elem), 1, (cuuint32_t)bsa::kTile};
   cuuint32_t estride[3] = {1, 1, 1};
@@ -124,7 +126,9 @@ namespace {
 bsa_status_t prefill(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
                      const int32_t *cu_seqlens_k, int32_t n_seqs, int32_t Hq, int32_t Hkv,
                      int32_t d, int32_t causal, float lambda, bsa_dtype_t dtype, void *out,
-                     float *lse, uint32_t *skip_bitmap, bsa_stream_t stream_) {
+                     float *lse, uint32_t *skip_bitmap, bsa_stream_t stream_,
+                     const int32_t *page_table = nullptr, int32_t max_pages = 0,
+                     int32_t num_pages = 0) {
   // ---- host-only checks: nothing is enqueued on failure
   if (!q || !k || !v || !cu_seqlens || !cu_seqlens_k || !out) return BSA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
@@ -150,15 +154,16 @@ bsa_status_t prefill(const void *q, const void *k, const void *v, const int32_t 
   if (!encoder()) return BSA_ERR_CUDA;
 
   CUtensorMap tmpl[3];
-  if (!encode_tile_map(&tmpl[0], q, Hq, fp8) || !encode_tile_map(&tmpl[1], k, Hkv, fp8) ||
-      !encode_tile_map(&tmpl[2], v, Hkv, fp8))
+  const uint64_t kv_tokens = page_table ? (uint64_t)num_pages * bsa::kTile : 1;
+  if (!encode_tile_map(&tmpl[0], q, Hq, fp8) || !encode_tile_map(&tmpl[1], k, Hkv, fp8, kv_tokens) ||
+      !encode_tile_map(&tmpl[2], v, Hkv, fp8, kv_tokens))
     return BSA_ERR_INVALID_ARG;
 
   const WorkspaceLayout layout = WorkspaceLayout::make(n_seqs);
   Workspace *ws = nullptr;
   if ((st = scratch_for(dev, stream, layout.bytes, &ws)) != BSA_OK) return st;
-  if (bsa::launch_prologue(cu_seqlens, cu_seqlens_k, n_seqs, Hq, Hkv, causal, ws, layout, tmpl,
-                           stream) != cudaSuccess)
+  if (bsa::launch_prologue(cu_seqlens, cu_seqlens_k, n_seqs, Hq, Hkv, causal, page_table,
+                           max_pages, num_pages, ws, layout, tmpl, stream) != cudaSuccess)
     return BSA_ERR_CUDA;
 
   char *base = reinterpret_cast<char *>(ws);
@@ -169,6 +174,8 @@ bsa_status_t prefill(const void *q, const void *k, const void *v, const int32_t 
   p.level_start = reinterpret_cast<const int32_t *>(base + layout.level_start);
   p.cu_seqlens = cu_seqlens;
   p.cu_seqlens_k = cu_seqlens_k;
+  p.page_table = page_table;
+  p.max_pages = page_table ? max_pages : 0;
   p.out = out;
   p.lse = lse;
   p.bitmap = skip_bitmap;
@@ -208,6 +215,21 @@ bsa_status_t bsa_prefill_fwd_chunked(const void *q, const void *k, const void *v
                                      float *lse, uint32_t *skip_bitmap, bsa_stream_t stream) {
   return prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, n_seqs, Hq, Hkv, d, causal, lambda, dtype,
                  out, lse, skip_bitmap, stream);
+}
+
+bsa_status_t bsa_prefill_fwd_paged(const void *q, const void *k_cache, const void *v_cache,
+                                   const int32_t *page_table, int32_t max_pages_per_seq,
+                                   int32_t num_pages, const int32_t *cu_seqlens_q,
+                                   const int32_t *cu_seqlens_k, int32_t n_seqs, int32_t Hq,
+                                   int32_t Hkv, int32_t d, int32_t causal, float lambda,
+                                   bsa_dtype_t dtype, void *out, float *lse,
+                                   uint32_t *skip_bitmap, bsa_stream_t stream) {
+  if (!page_table || !aligned(page_table, 4) || max_pages_per_seq < 1 || num_pages < 1 ||
+      (int64_t)num_pages * bsa::kTile > INT32_MAX)
+    return BSA_ERR_INVALID_ARG;
+  return prefill(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, n_seqs, Hq, Hkv, d, causal,
+                 lambda, dtype, out, lse, skip_bitmap, stream, page_table, max_pages_per_seq,
+                 num_pages);
 }
 
 bsa_status_t bsa_set_fp8_scales(const float *q_scale, const float *k_scale,

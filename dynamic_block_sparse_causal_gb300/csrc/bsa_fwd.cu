@@ -57,7 +57,8 @@ __device__ __forceinline__ int q_tiles(const int32_t *cu, int s) {
 
 __global__ void __launch_bounds__(1024)
 prologue_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ cuk, int n_seqs,
-                int Hq, int Hkv, int causal, Workspace *ws, int32_t *seq_sorted,
+                int Hq, int Hkv, int causal, const int32_t *__restrict__ page_table,
+                int max_pages, int num_pages, Workspace *ws, int32_t *seq_sorted,
                 int64_t *seq_bitmap_off, int32_t *level_start,
                 const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv) {
@@ -73,6 +74,17 @@ prologue_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ cuk,
     // queries are the last Lq positions of a sequence of Lk keys
     if (Lq < 0 || Lk < 0 || (causal && Lk < Lq) || (Lq > 0 && Lk == 0)) atomicOr(&s_bad, 1);
     atomicMax(&s_maxn, (Lq + kTile - 1) / kTile);
+    if (page_table && Lk > 0) {   // every page a sequence reads must exist
+      const int nk = (Lk + kTile - 1) / kTile;
+      if (nk > max_pages) {
+        atomicOr(&s_bad, 1);
+      } else {
+        for (int j = 0; j < nk; ++j) {
+          const int pg = page_table[(size_t)s * max_pages + j];
+          if (pg < 0 || pg >= num_pages) atomicOr(&s_bad, 1);
+        }
+      }
+    }
   }
   __syncthreads();
   const int maxn = s_maxn;
@@ -114,7 +126,7 @@ prologue_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ cuk,
     ws->total_tokens = cu[n_seqs];
     if (bad) atomicOr(&ws->status, kStatusBadSeqlens);
   }
-  if (tid < 3) {
+  if (tid < 3) {   // paged K/V maps already span the whole page pool
     const CUtensorMap *src = tid == 0 ? &tq : (tid == 1 ? &tk : &tv);
     CUtensorMap *dst = &ws->tmap[tid];
     const uint64_t *s64 = reinterpret_cast<const uint64_t *>(src);
@@ -122,21 +134,24 @@ prologue_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ cuk,
 #pragma unroll
     for (int w = 0; w < 16; ++w) d64[w] = s64[w];
     // token extent: query tokens for the Q map, key tokens for K and V
-    const int T = max(tid == 0 ? cu[n_seqs] : cuk[n_seqs], 1);
-    asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 2, %1;" ::"l"(dst),
-                 "r"(T)
-                 : "memory");
+    if (tid == 0 || !page_table) {
+      const int T = max(tid == 0 ? cu[n_seqs] : cuk[n_seqs], 1);
+      asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 2, %1;" ::"l"(dst),
+                   "r"(T)
+                   : "memory");
+    }
     asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
   }
 }
 
 cudaError_t launch_prologue(const int32_t *cu_seqlens, const int32_t *cu_seqlens_k, int n_seqs,
-                            int Hq, int Hkv, int causal, Workspace *ws,
+                            int Hq, int Hkv, int causal, const int32_t *page_table,
+                            int max_pages, int num_pages, Workspace *ws,
                             const WorkspaceLayout &layout, const CUtensorMap tmpl[3],
                             cudaStream_t stream) {
   char *base = reinterpret_cast<char *>(ws);
   prologue_kernel<<<1, 1024, 0, stream>>>(
-      cu_seqlens, cu_seqlens_k, n_seqs, Hq, Hkv, causal, ws,
+      cu_seqlens, cu_seqlens_k, n_seqs, Hq, Hkv, causal, page_table, max_pages, num_pages, ws,
       reinterpret_cast<int32_t *>(base + layout.seq_sorted),
       reinterpret_cast<int64_t *>(base + layout.seq_bitmap_off),
       reinterpret_cast<int32_t *>(base + layout.level_start), tmpl[0], tmpl[1], tmpl[2]);
@@ -291,6 +306,12 @@ __device__ __forceinline__ float exp2_fma(float x) {
 #define BSA_SPIN_SOFTMAX 0
 #endif
 constexpr int kSpinIssuer = BSA_SPIN_ISSUER;
+
+// Pass 1 loads all 128 score columns before a single TMEM wait (1), or in
+// two halves of 64 with a wait each (0).
+#ifndef BSA_PASS1_ONE_WAIT
+#define BSA_PASS1_ONE_WAIT 0
+#endif
 constexpr int kSpinSoftmax = BSA_SPIN_SOFTMAX;
 
 // One in kFmaExpEvery exponentials of a row goes to exp2_fma (0: none).
@@ -370,6 +391,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     const int qlast = min(qi * kTile + kTile, L) - 1;   // last valid row of the query tile
     const int last = p.causal ? min((off + qlast) / kTile, nk - 1) : nk - 1;
     const bool has1 = h1 >= 0;
+    // first token row of key tile j: packed K/V, or its page of the pool
+    auto kv_row = [&](int j) -> int {
+      return p.page_table ? p.page_table[(size_t)s * p.max_pages + j] * kTile : ak + j * kTile;
+    };
     bool ok = true;
 
     if (warp == 0) {
@@ -392,7 +417,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             mbar_expect_tx(&bar[B_KF + st], C::kTileBytes);
             for (int b = 0; b < C::kBoxes; ++b)
               tma_load_3d(sptr + SM_K + st * kRegion + b * kBox, tk, &bar[B_KF + st],
-                          b * C::kBoxCols, kvh, ak + j * kTile);
+                          b * C::kBoxCols, kvh, kv_row(j));
             kc_last[st] = (int)kc;
           }
           ++kc;
@@ -403,7 +428,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             mbar_expect_tx(&bar[B_VF + vs], C::kTileBytes);
             for (int b = 0; b < C::kBoxes; ++b)
               tma_load_3d(sptr + SM_V + vs * kRegion + b * kBox, tv, &bar[B_VF + vs],
-                          b * C::kBoxCols, kvh, ak + j * kTile);
+                          b * C::kBoxCols, kvh, kv_row(j));
             vc_last[vs] = (int)vc;
             ++vc;
           }
@@ -423,7 +448,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           mbar_expect_tx(&bar[B_VF + vs], C::kTileBytes);
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_3d(sptr + SM_V + vs * kRegion + b * kBox, tv, &bar[B_VF + vs],
-                        b * C::kBoxCols, kvh, ak + j * kTile);
+                        b * C::kBoxCols, kvh, kv_row(j));
           vc_last[vs] = (int)vc;
           return true;
         };
@@ -552,6 +577,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             float acc[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) acc[k] = -INFINITY;
+#if BSA_PASS1_ONE_WAIT
+            uint32_t v0[32], v1[32], v2[32], v3[32];
+            tmem_ld32(tS + 0, v0);
+            tmem_ld32(tS + 32, v1);
+            tmem_ld32(tS + 64, v2);
+            tmem_ld32(tS + 96, v3);
+            tmem_wait_ld(v0);
+            reg_fence(v1);
+            reg_fence(v2);
+            reg_fence(v3);
+            if (diag || tailt) {
+              mask_chunk(v0, 0, diag, tailt, row, doff, j * kTile, Lk);
+              mask_chunk(v1, 1, diag, tailt, row, doff, j * kTile, Lk);
+              mask_chunk(v2, 2, diag, tailt, row, doff, j * kTile, Lk);
+              mask_chunk(v3, 3, diag, tailt, row, doff, j * kTile, Lk);
+            }
+            row_max64(acc, v0, v1);
+            row_max64(acc, v2, v3);
+#else
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               uint32_t v0[32], v1[32];
@@ -565,6 +609,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
               }
               row_max64(acc, v0, v1);
             }
+#endif
             rm = max3f(max3f(acc[0], acc[1], acc[2]), max3f(acc[3], acc[4], acc[5]),
                        fmaxf(acc[6], acc[7]));
           }
@@ -613,7 +658,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             m2 = mnew;
             // P = exp2(S c - m_ref), written over the S columns already read:
             // chunk ch (keys 32ch..32ch+31) goes to columns 16ch.. (bf16) or 8ch.. (e4m3)
-            const float nm = -mref;
+            // rows past the end of the queries: scores of -inf give P = 0
+            const float nm = valid ? -mref : -INFINITY;
             float psum[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) psum[k] = 0.f;
@@ -632,7 +678,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
                   const float xe = fmaf(__uint_as_float(v[e]), c, nm);
                   const bool on_fma = kFmaExpEvery > 0 && (e % (kFmaExpEvery > 0 ? kFmaExpEvery : 1)) ==
                                                               (kFmaExpEvery > 0 ? kFmaExpEvery - 1 : 0);
-                  const float pv = valid ? (on_fma ? exp2_fma(xe) : ex2_approx(xe)) : 0.f;
+                  const float pv = on_fma ? exp2_fma(xe) : ex2_approx(xe);
                   psum[e & 7] += pv;
                   return pv;
                 };

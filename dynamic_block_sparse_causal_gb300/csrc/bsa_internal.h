@@ -54,6 +54,8 @@ struct FwdParams {
   const int32_t *level_start;
   const int32_t *cu_seqlens;     // query boundaries
   const int32_t *cu_seqlens_k;   // key/value boundaries (== cu_seqlens unless chunked)
+  const int32_t *page_table;     // paged KV: [n_seqs, max_pages] physical page of key tile j
+  int32_t max_pages;             // row length of page_table (0: K/V are packed, not paged)
   void *out;                 // bf16 [T, Hq, d]
   float *lse;                // [Hq, T] or null
   uint32_t *bitmap;          // or null
@@ -70,8 +72,11 @@ struct FwdParams {
 };
 
 // Host-side launchers (bsa_fwd.cu).
+// page_table / max_pages / num_pages: paged K/V (page = one 128-token tile);
+// page_table == nullptr for packed K/V, whose token extent the prologue patches.
 cudaError_t launch_prologue(const int32_t *cu_seqlens, const int32_t *cu_seqlens_k, int n_seqs,
-                            int Hq, int Hkv, int causal, Workspace *ws,
+                            int Hq, int Hkv, int causal, const int32_t *page_table,
+                            int max_pages, int num_pages, Workspace *ws,
                             const WorkspaceLayout &layout, const CUtensorMap tmpl[3],
                             cudaStream_t stream);
 cudaError_t launch_forward(const FwdParams &p, bool fp8, int num_ctas, cudaStream_t stream);

@@ -139,7 +139,7 @@ extern "C" bsa_status_t bsa_prefill_fwd_noalloc(
   bsa::Workspace *ws = static_cast<bsa::Workspace *>(s->scratch);
   // The status word keeps the last call's bits: start this call from zero.
   if (cudaMemsetAsync(&ws->status, 0, sizeof(int32_t), stream) != cudaSuccess) return BSA_ERR_CUDA;
-  if (bsa::launch_prologue(cu_seqlens, cu_seqlens, n_seqs, Hq, Hkv, causal, ws, kLayout, tmpl, stream) != cudaSuccess)
+  if (bsa::launch_prologue(cu_seqlens, cu_seqlens, n_seqs, Hq, Hkv, causal, nullptr, 0, 0, ws, kLayout, tmpl, stream) != cudaSuccess)
     return BSA_ERR_CUDA;
 
   char *base = static_cast<char *>(s->scratch);
@@ -150,6 +150,8 @@ extern "C" bsa_status_t bsa_prefill_fwd_noalloc(
   p.level_start = reinterpret_cast<const int32_t *>(base + kLayout.level_start);
   p.cu_seqlens = cu_seqlens;
   p.cu_seqlens_k = cu_seqlens;
+  p.page_table = nullptr;
+  p.max_pages = 0;
   p.out = out;
   p.lse = lse;
   p.bitmap = skip_bitmap;

@@ -137,6 +137,35 @@ bsa_status_t bsa_prefill_fwd_chunked(const void *q, const void *k, const void *v
                                      uint32_t *skip_bitmap, bsa_stream_t stream);
 
 /*
+ * Paged KV cache: chunked prefill whose keys and values are read from a pool
+ * of 128-token pages through a page table -- the paged KV cache that the
+ * deployment guide's §5 step 4 recommends for long contexts and that the
+ * block-sparse prefill monitoring page lists as a production requirement
+ * (FlashPrefill V2). A page holds one 128-key tile, so key tile j of
+ * sequence s is page page_table[s * max_pages_per_seq + j] of the pool.
+ *
+ * k_cache, v_cache  device [num_pages, 128, Hkv, d] (d fastest), 16-byte
+ *              aligned; only the pages a sequence uses are read.
+ * page_table   device int32 [n_seqs, max_pages_per_seq]; entries for the
+ *              ceil(Lk/128) tiles of each sequence must lie in
+ *              [0, num_pages) (checked on the device: BSA_ERR_BAD_SEQLENS,
+ *              nothing written); later entries are ignored.
+ * cu_seqlens_k device int32 [n_seqs + 1]: prefix sums of the key counts Lk
+ *              (used for lengths only; keys live in the pages).
+ * Everything else as bsa_prefill_fwd_chunked (queries are the last Lq of
+ * Lk positions; bitmap layout and size as there).
+ */
+bsa_status_t bsa_prefill_fwd_paged(const void *q, const void *k_cache,
+                                   const void *v_cache, const int32_t *page_table,
+                                   int32_t max_pages_per_seq, int32_t num_pages,
+                                   const int32_t *cu_seqlens_q,
+                                   const int32_t *cu_seqlens_k, int32_t n_seqs,
+                                   int32_t Hq, int32_t Hkv, int32_t d,
+                                   int32_t causal, float lambda,
+                                   bsa_dtype_t dtype, void *out, float *lse,
+                                   uint32_t *skip_bitmap, bsa_stream_t stream);
+
+/*
  * Same forward pass as bsa_prefill_fwd, same arguments and results, for
  * callers that may not allocate device memory -- for example a serving
  * engine that reserves nearly all of HBM for its own pool up front and

@@ -105,6 +105,20 @@ def test_chunked_argument_checks(L):
     assert L.prefill_fwd_chunked(*(args[:8] + (64,) + args[9:])) == 2      # d != 128
 
 
+def test_paged_argument_checks(L):
+    a = dict(q=16, k=32, v=48, pt=64, mp=4, npg=10, cuq=80, cuk=96, n=1, Hq=4, Hkv=2, d=128, c=1,
+             lam=0.01, dt=0, out=112, lse=None, bm=None)
+
+    def call(**o):
+        b = dict(a, **o)
+        return L.prefill_fwd_paged(b["q"], b["k"], b["v"], b["pt"], b["mp"], b["npg"], b["cuq"],
+                                   b["cuk"], b["n"], b["Hq"], b["Hkv"], b["d"], b["c"], b["lam"],
+                                   b["dt"], b["out"], b["lse"], b["bm"])
+    assert call(pt=None) == 1 and call(pt=66) == 1 and call(mp=0) == 1 and call(npg=0) == 1
+    assert call(npg=1 << 24) == 1           # pool larger than a 32-bit token index
+    assert call(cuk=None) == 1 and call(lam=2.0) == 1 and call(d=96) == 2
+
+
 def test_bitmap_words_rejects_bad_seqlens(L):
     assert L.skip_bitmap_words(np.array([1, 5], np.int32), 1) == -1
     assert L.skip_bitmap_words(np.array([0, 5, 3], np.int32), 1) == -1

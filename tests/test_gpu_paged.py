@@ -1,0 +1,100 @@
+"""GPU parity for the paged KV cache (bsa_prefill_fwd_paged).
+
+Keys and values are scattered over a pool of 128-token pages in a shuffled
+order (unused pages and the unused tail of each sequence's last page hold
+finite junk); the page table maps each sequence's key tiles to pages. The
+paged call must give exactly the results of the packed chunked call on the
+same data, and match the oracle; a page index outside the pool is rejected
+on the device.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import _cases
+import _gpu
+from gen import inputs as gi
+
+pytestmark = pytest.mark.gpu
+
+
+def page_pool(p, extra_pages=5, seed=0):
+    """Scatter p's packed K/V (by cu_seqlens_k) into shuffled 128-token pages."""
+    rng = np.random.default_rng(seed)
+    cuk = p.cu_seqlens_k if p.cu_seqlens_k is not None else p.cu_seqlens
+    lens = np.diff(cuk.astype(np.int64))
+    nk = (lens + 127) // 128
+    num_pages = int(nk.sum()) + extra_pages
+    max_pages = int(nk.max()) + 2
+    order = rng.permutation(num_pages)
+    junk = gi.bf16_bits_from_f32(rng.standard_normal((num_pages, 128, p.Hkv, p.d), dtype=np.float32))
+    kc, vc = junk.copy(), junk[::-1].copy()
+    table = np.full((len(lens), max_pages), -1, np.int32)
+    nxt = 0
+    for s, L in enumerate(lens):
+        a = int(cuk[s])
+        for j in range(int(nk[s])):
+            pg = int(order[nxt])
+            nxt += 1
+            table[s, j] = pg
+            t0, t1 = j * 128, min(j * 128 + 128, int(L))
+            kc[pg, :t1 - t0] = p.k[a + t0:a + t1]
+            vc[pg, :t1 - t0] = p.v[a + t0:a + t1]
+    return kc, vc, table, num_pages, max_pages
+
+
+def run_paged(p, pool, lam, causal=True):
+    b = _gpu.bsa()
+    kc, vc, table, num_pages, max_pages = pool
+    cuk = p.cu_seqlens_k if p.cu_seqlens_k is not None else p.cu_seqlens
+    T = p.total_tokens
+    q = _gpu.to_dev_bf16(p.q)
+    kd, vd = _gpu.to_dev_bf16(kc), _gpu.to_dev_bf16(vc)
+    pt = torch.from_numpy(table).cuda()
+    cq = torch.from_numpy(p.cu_seqlens.astype(np.int32)).cuda()
+    ck = torch.from_numpy(cuk.astype(np.int32)).cuda()
+    out = torch.full((T, p.Hq, p.d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((p.Hq, T), float("nan"), dtype=torch.float32, device="cuda")
+    nw = b.skip_bitmap_words_chunked(p.cu_seqlens, cuk, p.Hq)
+    bm = torch.full((max(nw, 1),), -1, dtype=torch.int32, device="cuda")
+    st = b.prefill_fwd_paged(q, kd, vd, pt, max_pages, num_pages, cq, ck, p.n_seqs, p.Hq, p.Hkv,
+                             p.d, int(causal), lam, b.BSA_BF16, out, lse, bm)
+    b.check(st, "bsa_prefill_fwd_paged")
+    torch.cuda.synchronize()
+    b.check(b.get_device_status(), "device status")
+    return dict(out=out, lse=lse, bitmap=bm[:nw].cpu().numpy().view(np.uint32), lam=lam,
+                causal=causal)
+
+
+CASES = [("gqa_ragged", [100, 777, 1, 200]), ("weak_sink", [384, 900]), ("gqa4", [1536, 777])]
+
+
+@pytest.mark.parametrize("key,lq", CASES)
+@pytest.mark.parametrize("lam", [0.01, 0.0, 0.3])
+@pytest.mark.parametrize("causal", [True, False])
+def test_paged_equals_packed_and_matches_oracle(key, lq, lam, causal):
+    base = _cases.small_problem(key)
+    p = gi.chunk(base, lq)
+    g = run_paged(p, page_pool(p, seed=len(lq)), lam, causal)
+    ref = _gpu.run(p, lam=lam, causal=causal)
+    assert torch.equal(g["out"], ref["out"]) and torch.equal(g["lse"], ref["lse"])
+    assert np.array_equal(g["bitmap"], ref["bitmap"])
+    _gpu.compare(p, g)
+
+
+def test_paged_rejects_page_outside_pool():
+    b = _gpu.bsa()
+    p = gi.chunk(_cases.small_problem("weak_sink"), [384, 900])
+    kc, vc, table, num_pages, max_pages = page_pool(p)
+    table[1, 3] = num_pages           # one past the pool
+    g_out = torch.full((p.total_tokens, p.Hq, p.d), 5.0, dtype=torch.bfloat16, device="cuda")
+    st = b.prefill_fwd_paged(_gpu.to_dev_bf16(p.q), _gpu.to_dev_bf16(kc), _gpu.to_dev_bf16(vc),
+                             torch.from_numpy(table).cuda(), max_pages, num_pages,
+                             torch.from_numpy(p.cu_seqlens).cuda(),
+                             torch.from_numpy(p.cu_seqlens_k).cuda(), p.n_seqs, p.Hq, p.Hkv, p.d,
+                             1, 0.01, b.BSA_BF16, g_out, None, None)
+    assert st == 0
+    assert b.get_device_status() == 6
+    assert bool((g_out == 5.0).all())
