@@ -64,6 +64,44 @@ def popcount(words: np.ndarray) -> int:
     return int(np.unpackbits(np.ascontiguousarray(words).view(np.uint8)).sum())
 
 
+# ------------------------------------------------------------------ measured DRAM traffic
+
+KERNEL_SOURCES = ("dynamic_block_sparse_causal_gb300/csrc/bsa_fwd.cu",
+                  "dynamic_block_sparse_causal_gb300/csrc/ptx.cuh",
+                  "dynamic_block_sparse_causal_gb300/csrc/bsa_internal.h")
+DRAM_PROFILE = os.path.join(ROOT, "profiles", "fwd_kernel_c2_dram.md")
+
+
+def kernel_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic():
+    """DRAM bytes per forward launch on the 128K layer, from the committed
+    single-pass ncu capture -- only if it was taken on the current kernel
+    sources (otherwise None: the counters no longer describe this kernel)."""
+    try:
+        text = open(DRAM_PROFILE).read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith(("kernel_sources_sha256", "traffic_bytes_per_launch")):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_sources_sha256") != kernel_sources_sha256():
+        return None
+    try:
+        return int(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 # ------------------------------------------------------------------ distributed
 
 def dist_env():
@@ -167,6 +205,12 @@ def _oracle_item(args):
     t0 = time.perf_counter()
     tile_walk.walk_one(qs, ks, vs, [0, hi], 1, 1, True, 0.01, 1.0 / math.sqrt(128), (0, 0, i))
     return time.perf_counter() - t0
+
+
+def chunk_dense_flops(lq, lk, Hq, d=128):
+    """Dense causal FLOPs of lq queries at the last positions of lk keys."""
+    off = lk - lq
+    return Hq * 4.0 * d * (lq * (off + 1) + lq * (lq - 1) / 2.0)
 
 
 def item_dense_flops(i, d=128):
@@ -306,8 +350,10 @@ def gpu_arm(args, rank, world, local_rank):
         pass
     peak = peaks.get("bf16_tflops", 1900.0)
     achieved = xflops / (ms * 1e-3) / 1e12
+    traffic = measured_traffic() if args.config == "C2" else None
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "algorithmic_bytes": int(2 * (p.q.size + p.k.size + p.v.size + p.q.size) + 4 * Hq * T),
                 "peak_source": "MEASURED_PEAKS.json bf16_tflops (burst)" if "bf16_tflops" in peaks
                 else "fallback 1900 TFLOP/s", "flops_per_launch": xflops}
 
@@ -360,6 +406,52 @@ def gpu_arm(args, rank, world, local_rank):
         bsa.check(bsa.set_fp8_scales(None, None, None), "clear scales")
         bsa.check(bsa.get_device_status(stream), "device status")
         del codes, scales
+
+    # next rows: chunked prefill (the last 8192 queries against all keys) and
+    # the same chunk with K/V in a shuffled pool of 128-token pages
+    rows = None
+    if not args.no_rows and p.n_seqs == 1:
+        lq = 8192
+        qc = q[T - lq:]
+        cuq = torch.tensor([0, lq], dtype=torch.int32, device=dev)
+        outc = torch.empty((lq, Hq, d), dtype=torch.bfloat16, device=dev)
+        lsec = torch.empty((Hq, lq), dtype=torch.float32, device=dev)
+        nwc = bsa.skip_bitmap_words_chunked(np.array([0, lq]), p.cu_seqlens, Hq)
+        bmc = torch.empty((nwc,), dtype=torch.int32, device=dev)
+        n_pages = (T + TILE - 1) // TILE
+        perm = torch.from_numpy(np.random.default_rng(0).permutation(n_pages).astype(np.int32)).to(dev)
+        kpool = torch.empty((n_pages * TILE, Hkv, d), dtype=torch.bfloat16, device=dev)
+        vpool = torch.empty_like(kpool)
+        kpool.view(n_pages, TILE, Hkv, d)[perm.long()] = k.view(n_pages, TILE, Hkv, d)
+        vpool.view(n_pages, TILE, Hkv, d)[perm.long()] = v.view(n_pages, TILE, Hkv, d)
+        table = perm.view(1, n_pages)
+        cf = chunk_dense_flops(lq, T, Hq, d)
+
+        def chunked():
+            bsa.check(bsa.prefill_fwd_chunked(qc, k, v, cuq, cu, 1, Hq, Hkv, d, 1, args.lam,
+                                              bsa.BSA_BF16, outc, lsec, bmc, stream), "chunked")
+
+        def paged():
+            bsa.check(bsa.prefill_fwd_paged(qc, kpool, vpool, table, n_pages, n_pages, cuq, cu, 1,
+                                            Hq, Hkv, d, 1, args.lam, bsa.BSA_BF16, outc, lsec, bmc,
+                                            stream), "paged")
+        rows = {}
+        for name, fn in (("chunked_prefill", chunked), ("paged_kv", paged)):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            m = e0.elapsed_time(e1) / args.steps
+            rows[name] = {"workload": f"last {lq} queries of the layer against all {T} keys" +
+                          (", K/V in a shuffled pool of 128-token pages" if name == "paged_kv" else ""),
+                          "ms": round(m, 3), "dense_equiv_tflops": round(cf / m / 1e9, 1)}
+        bsa.check(bsa.get_device_status(stream), "device status")
+        del kpool, vpool
 
     # dense causal attention from the box's library (torch SDPA) on the same
     # shape: the comparison for the lambda = 0 path
@@ -449,7 +541,7 @@ def gpu_arm(args, rank, world, local_rank):
         "dense_equiv_tflop_per_step": round(dflops / 1e12, 3),
         "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
         "gpu_launches": 2 * args.steps, "lambda_sweep": sweep, "dense_reference": dense_ref,
-        "fp8": fp8,
+        "fp8": fp8, "next_rows": rows,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -507,6 +599,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true")
+    ap.add_argument("--no-rows", action="store_true", help="skip the chunked / paged legs")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds per reference step")
     args = ap.parse_args(argv)

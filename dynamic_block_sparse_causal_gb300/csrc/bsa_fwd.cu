@@ -89,7 +89,10 @@ prologue_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ cuk,
   __syncthreads();
   const int maxn = s_maxn;
   const int group = Hq / Hkv;
-  const long long U = (long long)Hkv * ((group + 1) / 2);  // work items per (sequence, tile)
+  // work items are ordered KV head by KV head (so CTAs running at the same time
+  // stream the same head's K tiles through L2), and within a head longest
+  // query tile first; U = items per (sequence, query tile) within one head
+  const long long U = (group + 1) / 2;
   bool bad = s_bad || maxn > kMaxLevels;
   if (!bad) {
     // longest first (query tiles), ties by sequence index
@@ -119,6 +122,7 @@ prologue_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ cuk,
       words += (long long)Hq * nq * ((nk + 31) / 32);
       items += U * nq;
     }
+    items *= Hkv;
     if (items > INT_MAX) bad = true;
     ws->counter = 0;
     ws->total_items = bad ? 0 : (int32_t)items;
@@ -236,19 +240,22 @@ __device__ void fetch_item(const FwdParams &p, int total_items, int maxn, int *d
     dst[0] = 0;
     return;
   }
-  int lo = 0, hi = maxn - 1;   // smallest level whose first item is <= k
+  // KV head major: items [g * per_head, (g + 1) * per_head) belong to head g
+  const int per_head = total_items / p.Hkv;
+  const int kvh = k / per_head;
+  const int kr = k - kvh * per_head;
+  int lo = 0, hi = maxn - 1;   // smallest level whose first item is <= kr
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if (p.level_start[mid] <= k)
+    if (p.level_start[mid] <= kr)
       hi = mid;
     else
       lo = mid + 1;
   }
-  const int U = p.Hkv * p.pairs_per_group;
-  const int r = k - p.level_start[lo];
+  const int U = p.pairs_per_group;
+  const int r = kr - p.level_start[lo];
   const int s = p.seq_sorted[r / U];
-  const int pidx = r % U;
-  const int kvh = pidx / p.pairs_per_group, pp = pidx % p.pairs_per_group;
+  const int pp = r % U;
   const int h0 = kvh * p.group + 2 * pp;
   const int a = p.cu_seqlens[s], ak = p.cu_seqlens_k[s];
   dst[0] = 1;

@@ -75,3 +75,28 @@ def test_chunked_rejects_fewer_keys_than_queries():
                                  out, None, None) == 0
     assert b.get_device_status() == 6
     assert bool((out == 3.0).all())
+
+
+@pytest.mark.parametrize("lq", [[1, 1], [3, 4], [1, 128]])
+@pytest.mark.parametrize("lam", [0.005, 0.0])
+def test_decode_shaped_queries(lq, lam):
+    """A few new queries per sequence against all earlier keys (decode /
+    speculative-decode shape, the deployment guide's §6.1 decode threshold)."""
+    p = gi.chunk(_cases.small_problem("weak_sink"), lq)
+    g = _gpu.run(p, lam=lam)
+    out, lse = _gpu.host(g)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    _gpu.compare(p, g)
+
+
+@pytest.mark.parametrize("key,lq", [("gqa_ragged", [100, 777, 1, 200]), ("weak_sink", [384, 900])])
+def test_chunked_fp8(key, lq):
+    import test_gpu_fp8
+    p = gi.chunk(_cases.small_problem(key), lq)
+    f8q = test_gpu_fp8.gpu_quantize(p.q)
+    f8k = test_gpu_fp8.gpu_quantize(p.k)
+    f8v = test_gpu_fp8.gpu_quantize(p.v)
+    f8 = (f8q[0], f8k[0], f8v[0], f8q[1], f8k[1], f8v[1])
+    g = _gpu.run(p, lam=0.05, fp8=f8)
+    assert bool(torch.isfinite(g["out"]).all())
+    _gpu.compare(p, g, fp8=f8)

@@ -71,3 +71,12 @@ def test_fp8_full_size_sampled():
     g = _gpu.run(p, lam=0.01, fp8=f8)
     assert bool(torch.isfinite(g["out"]).all())
     print(_gpu.compare(p, g, items=_gpu.sample_items(p, 12, seed=2), fp8=f8))
+
+
+def test_fp8_128k_layer_sampled():
+    """The FP8 variant of the 128K Llama-shaped layer, as the bench times it."""
+    p = gi.config("C4")
+    f8 = quantized(p)
+    g = _gpu.run(p, lam=0.01, fp8=f8)
+    assert bool(torch.isfinite(g["out"]).all())
+    print(_gpu.compare(p, g, items=_gpu.sample_items(p, 8, seed=4), fp8=f8))

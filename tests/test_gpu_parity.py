@@ -76,3 +76,31 @@ def test_packed_equals_separate():
         g = _gpu.run(one, lam=0.01)
         assert torch.equal(g["out"], whole["out"][a:b])
         assert torch.equal(g["lse"], whole["lse"][:, a:b])
+
+
+def test_two_streams_concurrently():
+    """Calls on two streams may overlap: each stream has its own scratch area."""
+    b = _gpu.bsa()
+    pa, pb = _cases.small_problem("gqa_ragged"), _cases.small_problem("weak_sink")
+    ref_a, ref_b = _gpu.run(pa, lam=0.01), _gpu.run(pb, lam=0.05)
+
+    def launch(p, lam, stream):
+        q, k, v = _gpu.to_dev_bf16(p.q), _gpu.to_dev_bf16(p.k), _gpu.to_dev_bf16(p.v)
+        cu = torch.from_numpy(p.cu_seqlens).cuda()
+        out = torch.empty((p.total_tokens, p.Hq, p.d), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((p.Hq, p.total_tokens), dtype=torch.float32, device="cuda")
+        bm = torch.empty((b.skip_bitmap_words(p.cu_seqlens, p.Hq),), dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        for _ in range(3):
+            b.check(b.prefill_fwd(q, k, v, cu, p.n_seqs, p.Hq, p.Hkv, p.d, 1, lam, b.BSA_BF16,
+                                  out, lse, bm, stream), "launch")
+        return out, lse, bm, (q, k, v, cu)
+
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    oa = launch(pa, 0.01, sa)
+    ob = launch(pb, 0.05, sb)
+    torch.cuda.synchronize()
+    assert b.get_device_status(sa) == 0 and b.get_device_status(sb) == 0
+    assert torch.equal(oa[0], ref_a["out"]) and torch.equal(ob[0], ref_b["out"])
+    assert np.array_equal(oa[2].cpu().numpy().view(np.uint32), ref_a["bitmap"])
+    assert np.array_equal(ob[2].cpu().numpy().view(np.uint32), ref_b["bitmap"])
