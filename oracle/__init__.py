@@ -19,10 +19,14 @@ Modules:
   skip rule, plus a mask-replay mode that consumes a given skip bitmap;
 * ``decisions`` -- a second, non-iterative statement of the skip decisions
   (prefix max of tile row maxima);
-* ``layout``    -- the skip-bitmap word layout of the C interface.
+* ``layout``    -- the skip-bitmap word layout of the C interface;
+* ``importance`` -- the UniPrefill block importance (Eq. 3-4) and top-p
+  block selection (§3.3), the second workload on the pages.
 
 Pins (what checks this code against something other than itself) live in
-``tests/test_oracle_pins.py``. Every function is pinned there; none is
-"parity unpinned".
+``tests/test_oracle_pins.py`` (attention, skip rule, formats, layout),
+``tests/test_oracle_chunked.py`` (query offsets) and
+``tests/test_oracle_importance.py`` (block importance, top-p). Every
+function is pinned; none is "parity unpinned".
 """
-from . import numerics, attention, tile_walk, decisions, layout  # noqa: F401
+from . import numerics, attention, tile_walk, decisions, layout, importance  # noqa: F401
