@@ -453,6 +453,81 @@ def gpu_arm(args, rank, world, local_rank):
         bsa.check(bsa.get_device_status(stream), "device status")
         del kpool, vpool
 
+        def time_fn(fn, n):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / n
+
+        # decode-shaped calls (one new query per sequence, the deployment
+        # guide's decode threshold 0.005): the whole 128K context, and the
+        # layer cut into four 32K contexts
+        hbm_peak = peaks.get("hbm_gbs", 6800.0)
+        for name, cuts in (("decode_1x128k", [0, T]), ("decode_4x32k", [0, T // 4, T // 2, 3 * T // 4, T])):
+            nseq = len(cuts) - 1
+            cuk_d = torch.tensor(cuts, dtype=torch.int32, device=dev)
+            cuq_d = torch.arange(nseq + 1, dtype=torch.int32, device=dev)
+            qd = torch.stack([q[c - 1] for c in cuts[1:]]).contiguous()
+            outd = torch.empty((nseq, Hq, d), dtype=torch.bfloat16, device=dev)
+            nwd = bsa.skip_bitmap_words_chunked(np.arange(nseq + 1), np.array(cuts), Hq)
+            bmd = torch.empty((nwd,), dtype=torch.int32, device=dev)
+
+            def dec():
+                bsa.check(bsa.prefill_fwd_chunked(qd, k, v, cuq_d, cuk_d, nseq, Hq, Hkv, d, 1, 0.005,
+                                                  bsa.BSA_BF16, outd, None, bmd, stream), "decode")
+            m = time_fn(dec, args.steps)
+            bits = bmd.cpu().numpy().view(np.uint32)
+            # bytes: every K tile once per KV head, V tiles that some query head kept
+            kv_tiles = sum((b - a + TILE - 1) // TILE for a, b in zip(cuts[:-1], cuts[1:]))
+            words = (np.array([(b - a + TILE - 1) // TILE for a, b in zip(cuts[:-1], cuts[1:])]) + 31) // 32
+            v_kept = 0
+            off = 0
+            for sq in range(nseq):
+                W, nt = int(words[sq]), (cuts[sq + 1] - cuts[sq] + TILE - 1) // TILE
+                rowsb = bits[off:off + Hq * W].reshape(Hq, W)
+                off += Hq * W
+                sk = np.unpackbits(rowsb.view(np.uint8), bitorder="little").reshape(Hq, -1)[:, :nt]
+                keep = (sk == 0).reshape(Hkv, Hq // Hkv, nt).any(axis=1)
+                v_kept += int(keep.sum())
+            tile_bytes = TILE * d * 2
+            nbytes = kv_tiles * Hkv * tile_bytes + v_kept * tile_bytes
+            gbs = nbytes / (m * 1e-3) / 1e9
+            rows[name] = {"workload": f"{nseq} sequence(s) x {T // nseq} keys, one new query each, lambda 0.005",
+                          "ms": round(m, 4), "kv_bytes": int(nbytes), "achieved_gbs": round(gbs, 1),
+                          "hbm_peak_gbs": hbm_peak, "hbm_frac": round(gbs / hbm_peak, 4),
+                          "v_tiles_kept": v_kept, "k_tiles": kv_tiles * Hkv}
+        bsa.check(bsa.get_device_status(stream), "device status")
+
+        # UniPrefill block importance of the layer (last 64 queries, G = 128)
+        # and the top-p (p = 0.9) selection over its head-mean scores
+        nb = bsa.importance_blocks(p.cu_seqlens)
+        sc = torch.empty((Hq, nb), dtype=torch.float32, device=dev)
+        mn = torch.empty((nb,), dtype=torch.float32, device=dev)
+        order = torch.empty((nb,), dtype=torch.int32, device=dev)
+        nsel = torch.empty((1,), dtype=torch.int32, device=dev)
+        keep = torch.empty((nb,), dtype=torch.uint8, device=dev)
+
+        def importance():
+            bsa.check(bsa.block_importance(q, k, cu, 1, Hq, Hkv, d, 64, 1, nb, sc, mn, stream), "importance")
+
+        def select():
+            bsa.check(bsa.top_p_select(mn, cu, 1, nb, 0.9, order, nsel, keep, stream), "top_p")
+        mi = time_fn(importance, args.steps)
+        ms_sel = time_fn(select, args.steps)
+        bsa.check(bsa.get_device_status(stream), "device status")
+        mma_flops = Hq * nb * 2 * TILE * TILE * d          # 128-row tiles issued
+        rows["block_importance"] = {
+            "workload": f"UniPrefill Eq. 3-4 on the layer: last 64 queries, {nb} blocks of 128 keys, {Hq} heads",
+            "ms": round(mi, 4), "top_p_ms": round(ms_sel, 4), "p": 0.9, "kept_blocks": int(nsel[0]),
+            "mma_tflops": round(mma_flops / mi / 1e9, 1), "mma_frac": round(mma_flops / mi / 1e9 / peak, 4),
+            "launches": 5}
+
     # dense causal attention from the box's library (torch SDPA) on the same
     # shape: the comparison for the lambda = 0 path
     dense_ref = None

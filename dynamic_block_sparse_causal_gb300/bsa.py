@@ -68,6 +68,12 @@ def lib() -> ctypes.CDLL:
     L.bsa_release.restype = None
     L.bsa_debug_fault_drill.argtypes = [i32, i64]
     L.bsa_debug_fault_drill.restype = i32
+    L.bsa_block_importance.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i64, vp, vp, vp]
+    L.bsa_block_importance.restype = i32
+    L.bsa_top_p_select.argtypes = [vp, vp, i32, i64, f32, vp, vp, vp, vp]
+    L.bsa_top_p_select.restype = i32
+    L.bsa_importance_blocks.argtypes = [ctypes.POINTER(ctypes.c_int32), i32]
+    L.bsa_importance_blocks.restype = i64
     _lib = L
     return L
 
@@ -151,6 +157,30 @@ def skip_bitmap_words_chunked(cu_seqlens_q_host, cu_seqlens_k_host, Hq) -> int:
     P = ctypes.POINTER(ctypes.c_int32)
     return lib().bsa_skip_bitmap_words_chunked(cq.ctypes.data_as(P), ck.ctypes.data_as(P),
                                                int(cq.shape[0] - 1), int(Hq))
+
+
+def block_importance(q, k, cu_seqlens, n_seqs, Hq, Hkv, d, n_window, causal, total_blocks,
+                     scores, mean_scores, stream=None) -> int:
+    """bsa_block_importance: per-head block scores of the last n_window queries."""
+    return lib().bsa_block_importance(_ptr(q), _ptr(k), _ptr(cu_seqlens), int(n_seqs), int(Hq),
+                                      int(Hkv), int(d), int(n_window), int(causal),
+                                      int(total_blocks), _ptr(scores), _ptr(mean_scores),
+                                      _stream(stream))
+
+
+def top_p_select(scores, cu_seqlens, n_seqs, total_blocks, p, order, n_selected, keep,
+                 stream=None) -> int:
+    """bsa_top_p_select: per-sequence block order by score and the top-p count."""
+    return lib().bsa_top_p_select(_ptr(scores), _ptr(cu_seqlens), int(n_seqs), int(total_blocks),
+                                  float(p), _ptr(order), _ptr(n_selected), _ptr(keep),
+                                  _stream(stream))
+
+
+def importance_blocks(cu_seqlens_host) -> int:
+    import numpy as np
+    cu = np.ascontiguousarray(cu_seqlens_host, dtype=np.int32)
+    return lib().bsa_importance_blocks(cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                       int(cu.shape[0] - 1))
 
 
 def get_device_status(stream=None) -> int:

@@ -12,6 +12,7 @@
 #include <utility>
 
 #include "bsa.h"
+#include "bsa_importance.h"
 #include "bsa_internal.h"
 
 namespace {
@@ -32,6 +33,12 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 std::map<std::pair<int, cudaStream_t>, StreamScratch> g_scratch;
+// block-importance tables per (device, stream), grown like the scratch area
+struct ImpScratch {
+  void *ptr = nullptr;
+  size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, ImpScratch> g_imp_scratch;
 std::map<int, DeviceInfo> g_devices;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -65,7 +72,9 @@ bsa_status_t device_info(int dev, DeviceInfo **out) {
         cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return BSA_ERR_CUDA;
     d.supported = (major == 10 && minor == 3);
-    if (d.supported && bsa::prepare_forward() != cudaSuccess) return BSA_ERR_CUDA;
+    if (d.supported &&
+        (bsa::prepare_forward() != cudaSuccess || bsa::prepare_importance() != cudaSuccess))
+      return BSA_ERR_CUDA;
     d.ready = true;
   }
   *out = &d;
@@ -89,6 +98,20 @@ bsa_status_t scratch_for(int dev, cudaStream_t stream, size_t bytes, Workspace *
     s.bytes = bytes;
   }
   *out = s.ws;
+  return BSA_OK;
+}
+
+// Block-importance tables of (device, stream), grown stream-ordered.
+bsa_status_t imp_scratch_for(int dev, cudaStream_t stream, size_t bytes, void **out) {
+  ImpScratch &s = g_imp_scratch[{dev, stream}];
+  if (s.bytes < bytes) {
+    void *p = nullptr;
+    if (cudaMallocAsync(&p, bytes, stream) != cudaSuccess) return BSA_ERR_NO_MEMORY;
+    if (s.ptr && cudaFreeAsync(s.ptr, stream) != cudaSuccess) return BSA_ERR_CUDA;
+    s.ptr = p;
+    s.bytes = bytes;
+  }
+  *out = s.ptr;
   return BSA_OK;
 }
 
@@ -232,6 +255,105 @@ bsa_status_t bsa_prefill_fwd_paged(const void *q, const void *k_cache, const voi
                  num_pages);
 }
 
+int64_t bsa_importance_blocks(const int32_t *cu, int32_t n_seqs) {
+  if (!cu || n_seqs < 1 || cu[0] != 0) return -1;
+  int64_t blocks = 0;
+  for (int32_t s = 0; s < n_seqs; ++s) {
+    const int64_t L = (int64_t)cu[s + 1] - cu[s];
+    if (L < 0) return -1;
+    blocks += (L + bsa::kTile - 1) / bsa::kTile;
+  }
+  return blocks;
+}
+
+bsa_status_t bsa_block_importance(const void *q, const void *k, const int32_t *cu_seqlens,
+                                  int32_t n_seqs, int32_t Hq, int32_t Hkv, int32_t d,
+                                  int32_t n_window, int32_t causal, int64_t total_blocks,
+                                  float *scores, float *mean_scores, bsa_stream_t stream_) {
+  if (!q || !k || !cu_seqlens || !scores) return BSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(cu_seqlens, 4) || !aligned(scores, 4) ||
+      !aligned(mean_scores, 4))
+    return BSA_ERR_INVALID_ARG;
+  if (n_seqs < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Hq > 65535 ||
+      (int64_t)n_seqs * Hq > INT_MAX)
+    return BSA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return BSA_ERR_INVALID_ARG;
+  if (n_window < 1 || n_window > bsa::kImpMaxWindow) return BSA_ERR_INVALID_ARG;
+  if (total_blocks < 0 || total_blocks > ((int64_t)1 << 40) / Hq) return BSA_ERR_INVALID_ARG;
+  if (d != bsa::kHeadDim) return BSA_ERR_UNSUPPORTED;
+
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo *info = nullptr;
+  bsa_status_t st = device_info(dev, &info);
+  if (st != BSA_OK) return st;
+  if (!info->supported) return BSA_ERR_UNSUPPORTED;
+  if (!encoder()) return BSA_ERR_CUDA;
+
+  CUtensorMap tmpl[2];
+  if (!encode_tile_map(&tmpl[0], q, Hq, false) || !encode_tile_map(&tmpl[1], k, Hkv, false))
+    return BSA_ERR_INVALID_ARG;
+  Workspace *ws = nullptr;   // holds the status word
+  if ((st = scratch_for(dev, stream, sizeof(Workspace), &ws)) != BSA_OK) return st;
+  const bsa::ImpLayout layout = bsa::ImpLayout::make(n_seqs, Hq, total_blocks);
+  void *buf = nullptr;
+  if ((st = imp_scratch_for(dev, stream, layout.bytes, &buf)) != BSA_OK) return st;
+  char *base = static_cast<char *>(buf);
+
+  bsa::ImpParams p{};
+  p.iw = static_cast<bsa::ImpWorkspace *>(buf);
+  p.ws = ws;
+  p.cu = cu_seqlens;
+  p.blk_off = reinterpret_cast<const int64_t *>(base + layout.blk_off);
+  p.item_off = reinterpret_cast<const int32_t *>(base + layout.item_off);
+  p.stat_t = reinterpret_cast<float *>(base + layout.stat_t);
+  p.stat_e = reinterpret_cast<float *>(base + layout.stat_e);
+  p.chunk_m = reinterpret_cast<float *>(base + layout.chunk_m);
+  p.chunk_l = reinterpret_cast<float *>(base + layout.chunk_l);
+  p.row_lse = reinterpret_cast<float *>(base + layout.row_lse);
+  p.max_chunks = layout.max_chunks;
+  p.scores = scores;
+  p.mean_scores = mean_scores;
+  p.total_blocks = total_blocks;
+  p.n_seqs = n_seqs;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.group = Hq / Hkv;
+  p.n_window = n_window;
+  p.causal = causal;
+  p.c = (float)(1.0 / std::sqrt((double)d) * 1.4426950408889634);
+  p.wait_limit_ns = t_wait_limit_ns;
+  if (bsa::launch_importance(p, tmpl, info->sm_count, stream) != cudaSuccess) return BSA_ERR_CUDA;
+  return BSA_OK;
+}
+
+bsa_status_t bsa_top_p_select(const float *scores, const int32_t *cu_seqlens, int32_t n_seqs,
+                              int64_t total_blocks, float p, int32_t *order, int32_t *n_selected,
+                              uint8_t *keep, bsa_stream_t stream_) {
+  if (!scores || !cu_seqlens || !order || !n_selected) return BSA_ERR_INVALID_ARG;
+  if (!aligned(scores, 4) || !aligned(cu_seqlens, 4) || !aligned(order, 4) ||
+      !aligned(n_selected, 4))
+    return BSA_ERR_INVALID_ARG;
+  if (n_seqs < 1 || total_blocks < 0) return BSA_ERR_INVALID_ARG;
+  if (!(p > 0.0f && p <= 1.0f)) return BSA_ERR_INVALID_ARG;   // also rejects NaN
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo *info = nullptr;
+  bsa_status_t st = device_info(dev, &info);
+  if (st != BSA_OK) return st;
+  if (!info->supported) return BSA_ERR_UNSUPPORTED;
+  Workspace *ws = nullptr;
+  if ((st = scratch_for(dev, stream, sizeof(Workspace), &ws)) != BSA_OK) return st;
+  if (bsa::launch_top_p(scores, cu_seqlens, n_seqs, total_blocks, p, order, n_selected, keep, ws,
+                        stream) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  return BSA_OK;
+}
+
 bsa_status_t bsa_set_fp8_scales(const float *q_scale, const float *k_scale,
                                 const float *v_scale) {
   const int nulls = !q_scale + !k_scale + !v_scale;
@@ -324,6 +446,13 @@ void bsa_release(void) {
     }
   }
   g_scratch.clear();
+  for (auto &kv : g_imp_scratch) {
+    if (kv.second.ptr) {
+      cudaSetDevice(kv.first.first);
+      cudaFree(kv.second.ptr);
+    }
+  }
+  g_imp_scratch.clear();
   cudaSetDevice(cur);
 }
 

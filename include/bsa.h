@@ -230,6 +230,72 @@ int64_t bsa_skip_bitmap_words_chunked(const int32_t *cu_seqlens_q_host,
                                       int32_t n_seqs, int32_t Hq);
 
 /*
+ * Token-block importance ("UniPrefill：通过分块动态稀疏化实现通用长上下文预填充
+ * 加速", §3.2 Eq. (3)-(4)). For every sequence and query head h, the attention
+ * weights A[j, i] of the last n = min(n_window, L) query positions j over
+ * the sequence's keys i, with the softmax (scale 1/sqrt(d)) normalised over
+ * the whole key range, are averaged over the n rows and summed over blocks
+ * of G = 128 keys:
+ *
+ *        score[h, g] = (1 / (n G)) * sum_{i in block g} sum_j A[j, i].
+ *
+ * Row j attends the keys i <= j when causal = 1 and every key of the
+ * sequence when causal = 0. A sequence's block scores of one head add up to
+ * 1/G. Readings where the page is silent: G = 128 (this library's tile), the
+ * division by G also for a short last block (as Eq. 4 writes it), one score
+ * row per query head (GQA: head h reads key head h / (Hq / Hkv)).
+ *
+ * q, k         device bfloat16 [total_tokens, Hq | Hkv, d], 16-byte aligned.
+ * cu_seqlens   device int32 [n_seqs + 1], as for bsa_prefill_fwd.
+ * d            128 only. n_window 1..128. causal 0 or 1.
+ * total_blocks sum over sequences of ceil(L_s / 128), from
+ *              bsa_importance_blocks(); checked on the device against
+ *              cu_seqlens (a mismatch writes nothing and records
+ *              BSA_ERR_BAD_SEQLENS).
+ * scores       device float32 [Hq, total_blocks]; sequence s's blocks start
+ *              at column sum_{t<s} ceil(L_t / 128).
+ * mean_scores  device float32 [total_blocks] or NULL: the mean over query
+ *              heads, the score the selection below ranks.
+ * Scratch (two float tables of Hq x total_blocks x 128) is library-owned,
+ * per stream, grown stream-ordered.
+ */
+bsa_status_t bsa_block_importance(const void *q, const void *k,
+                                  const int32_t *cu_seqlens, int32_t n_seqs,
+                                  int32_t Hq, int32_t Hkv, int32_t d,
+                                  int32_t n_window, int32_t causal,
+                                  int64_t total_blocks, float *scores,
+                                  float *mean_scores, bsa_stream_t stream);
+
+/*
+ * Top-p block selection (same page, §3.3): per sequence, the block indices
+ * sorted by descending score (ties: ascending index) and the smallest k*
+ * such that the running sum of the first k* sorted scores reaches p times
+ * the sum of all of them (running sums in double precision; the total is
+ * the running sum at the last block).
+ *
+ * scores       device float32 [total_blocks] (finite, >= 0), laid out as
+ *              bsa_block_importance's mean_scores.
+ * cu_seqlens   device int32 [n_seqs + 1]; every sequence may have at most
+ *              16384 blocks (2M tokens), else nothing is written and
+ *              BSA_ERR_BAD_SEQLENS is recorded.
+ * p            0 < p <= 1 (NaN rejected).
+ * order        device int32 [total_blocks]: order[off_s + r] = block index
+ *              (within sequence s) of rank r.
+ * n_selected   device int32 [n_seqs]: k* (0 for an empty sequence).
+ * keep         device uint8 [total_blocks] or NULL: 1 for a kept block.
+ */
+bsa_status_t bsa_top_p_select(const float *scores, const int32_t *cu_seqlens,
+                              int32_t n_seqs, int64_t total_blocks, float p,
+                              int32_t *order, int32_t *n_selected,
+                              uint8_t *keep, bsa_stream_t stream);
+
+/*
+ * Number of 128-token blocks of a batch, sum of ceil(L_s / 128), from a HOST
+ * copy of cu_seqlens. -1 for a malformed cu_seqlens or n_seqs < 1.
+ */
+int64_t bsa_importance_blocks(const int32_t *cu_seqlens_host, int32_t n_seqs);
+
+/*
  * Synchronises `stream`, returns the device-side status recorded by the
  * calls made on it since the last read (BSA_OK, BSA_ERR_BAD_SEQLENS or
  * BSA_ERR_TIMEOUT) and clears it. BSA_ERR_CUDA if the synchronisation

@@ -119,6 +119,40 @@ def test_paged_argument_checks(L):
     assert call(cuk=None) == 1 and call(lam=2.0) == 1 and call(d=96) == 2
 
 
+def test_importance_argument_checks(L):
+    a = dict(q=16, k=32, cu=64, n=1, Hq=4, Hkv=2, d=128, nw=64, c=1, tb=10, sc=80, mean=None)
+
+    def call(**o):
+        b = dict(a, **o)
+        return L.block_importance(b["q"], b["k"], b["cu"], b["n"], b["Hq"], b["Hkv"], b["d"],
+                                  b["nw"], b["c"], b["tb"], b["sc"], b["mean"])
+    assert call(q=None) == 1 and call(k=None) == 1 and call(cu=None) == 1 and call(sc=None) == 1
+    assert call(q=24) == 1 and call(cu=66) == 1 and call(sc=82) == 1 and call(mean=83) == 1
+    assert call(n=0) == 1 and call(Hq=6, Hkv=4) == 1 and call(c=2) == 1
+    assert call(nw=0) == 1 and call(nw=129) == 1 and call(tb=-1) == 1
+    assert call(d=64) == 2
+
+
+def test_top_p_argument_checks(L):
+    a = dict(sc=16, cu=32, n=1, tb=10, p=0.9, order=48, nsel=64, keep=None)
+
+    def call(**o):
+        b = dict(a, **o)
+        return L.top_p_select(b["sc"], b["cu"], b["n"], b["tb"], b["p"], b["order"], b["nsel"],
+                              b["keep"])
+    assert call(sc=None) == 1 and call(cu=None) == 1 and call(order=None) == 1
+    assert call(nsel=None) == 1 and call(order=50) == 1 and call(n=0) == 1 and call(tb=-1) == 1
+    for bad_p in (0.0, -0.5, 1.0000001, 2.0, math.nan, math.inf):
+        assert call(p=bad_p) == 1
+
+
+@pytest.mark.parametrize("cu", [[0, 2048], [0, 300, 5000], [0, 1, 78, 206], [0, 0, 129, 129]])
+def test_importance_blocks_match_oracle(L, cu):
+    from oracle import importance
+    assert L.importance_blocks(np.array(cu, np.int32)) == int(importance.block_offsets(cu)[-1])
+    assert L.importance_blocks(np.array([0, 5, 3], np.int32)) == -1
+
+
 def test_bitmap_words_rejects_bad_seqlens(L):
     assert L.skip_bitmap_words(np.array([1, 5], np.int32), 1) == -1
     assert L.skip_bitmap_words(np.array([0, 5, 3], np.int32), 1) == -1
