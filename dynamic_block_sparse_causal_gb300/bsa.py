@@ -68,6 +68,9 @@ def lib() -> ctypes.CDLL:
     L.bsa_release.restype = None
     L.bsa_debug_fault_drill.argtypes = [i32, i64]
     L.bsa_debug_fault_drill.restype = i32
+    L.bsa_decode_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32, i32, f32, vp,
+                                 vp, vp, vp]
+    L.bsa_decode_fwd.restype = i32
     L.bsa_block_importance.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i64, vp, vp, vp]
     L.bsa_block_importance.restype = i32
     L.bsa_top_p_select.argtypes = [vp, vp, i32, i64, f32, vp, vp, vp, vp]
@@ -157,6 +160,15 @@ def skip_bitmap_words_chunked(cu_seqlens_q_host, cu_seqlens_k_host, Hq) -> int:
     P = ctypes.POINTER(ctypes.c_int32)
     return lib().bsa_skip_bitmap_words_chunked(cq.ctypes.data_as(P), ck.ctypes.data_as(P),
                                                int(cq.shape[0] - 1), int(Hq))
+
+
+def decode_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, n_seqs, max_seqlen_q, total_k, Hq, Hkv, d,
+               causal, lam, out, lse, skip_bitmap, stream=None) -> int:
+    """bsa_decode_fwd: a few new queries per sequence against all earlier keys (split-KV)."""
+    return lib().bsa_decode_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                int(n_seqs), int(max_seqlen_q), int(total_k), int(Hq), int(Hkv),
+                                int(d), int(causal), float(lam), _ptr(out), _ptr(lse),
+                                _ptr(skip_bitmap), _stream(stream))
 
 
 def block_importance(q, k, cu_seqlens, n_seqs, Hq, Hkv, d, n_window, causal, total_blocks,

@@ -12,6 +12,7 @@
 #include <utility>
 
 #include "bsa.h"
+#include "bsa_decode.h"
 #include "bsa_importance.h"
 #include "bsa_internal.h"
 
@@ -39,6 +40,7 @@ struct ImpScratch {
   size_t bytes = 0;
 };
 std::map<std::pair<int, cudaStream_t>, ImpScratch> g_imp_scratch;
+std::map<std::pair<int, cudaStream_t>, ImpScratch> g_dec_scratch;   // decode tables
 std::map<int, DeviceInfo> g_devices;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -73,7 +75,8 @@ bsa_status_t device_info(int dev, DeviceInfo **out) {
       return BSA_ERR_CUDA;
     d.supported = (major == 10 && minor == 3);
     if (d.supported &&
-        (bsa::prepare_forward() != cudaSuccess || bsa::prepare_importance() != cudaSuccess))
+        (bsa::prepare_forward() != cudaSuccess || bsa::prepare_importance() != cudaSuccess ||
+         bsa::prepare_decode() != cudaSuccess))
       return BSA_ERR_CUDA;
     d.ready = true;
   }
@@ -101,9 +104,10 @@ bsa_status_t scratch_for(int dev, cudaStream_t stream, size_t bytes, Workspace *
   return BSA_OK;
 }
 
-// Block-importance tables of (device, stream), grown stream-ordered.
-bsa_status_t imp_scratch_for(int dev, cudaStream_t stream, size_t bytes, void **out) {
-  ImpScratch &s = g_imp_scratch[{dev, stream}];
+// Block-importance or decode tables of (device, stream), grown stream-ordered.
+bsa_status_t imp_scratch_for(int dev, cudaStream_t stream, size_t bytes, void **out,
+                             std::map<std::pair<int, cudaStream_t>, ImpScratch> &pool = g_imp_scratch) {
+  ImpScratch &s = pool[{dev, stream}];
   if (s.bytes < bytes) {
     void *p = nullptr;
     if (cudaMallocAsync(&p, bytes, stream) != cudaSuccess) return BSA_ERR_NO_MEMORY;
@@ -253,6 +257,81 @@ bsa_status_t bsa_prefill_fwd_paged(const void *q, const void *k_cache, const voi
   return prefill(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, n_seqs, Hq, Hkv, d, causal,
                  lambda, dtype, out, lse, skip_bitmap, stream, page_table, max_pages_per_seq,
                  num_pages);
+}
+
+bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
+                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                            int32_t n_seqs, int32_t max_seqlen_q, int64_t total_k, int32_t Hq,
+                            int32_t Hkv, int32_t d, int32_t causal, float lambda, void *out,
+                            float *lse, uint32_t *skip_bitmap, bsa_stream_t stream_) {
+  if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out) return BSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4) || !aligned(lse, 4) ||
+      !aligned(skip_bitmap, 4))
+    return BSA_ERR_INVALID_ARG;
+  if (n_seqs < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Hq > 65535) return BSA_ERR_INVALID_ARG;
+  const int group = Hq / Hkv;
+  if (group > 16 || max_seqlen_q < 1 || (int64_t)group * max_seqlen_q > bsa::kDecMaxRows)
+    return BSA_ERR_INVALID_ARG;
+  if ((int64_t)n_seqs * max_seqlen_q * Hq > INT_MAX || (int64_t)n_seqs * Hkv > INT_MAX)
+    return BSA_ERR_INVALID_ARG;
+  if (total_k < 0 || total_k > INT_MAX - 2 * bsa::kTile) return BSA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return BSA_ERR_INVALID_ARG;
+  if (!(lambda >= 0.0f && lambda < 1.0f)) return BSA_ERR_INVALID_ARG;
+  if (d != bsa::kHeadDim) return BSA_ERR_UNSUPPORTED;
+
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo *info = nullptr;
+  bsa_status_t st = device_info(dev, &info);
+  if (st != BSA_OK) return st;
+  if (!info->supported) return BSA_ERR_UNSUPPORTED;
+  if (!encoder()) return BSA_ERR_CUDA;
+  CUtensorMap tk, tv;
+  const uint64_t extent = total_k > 0 ? (uint64_t)total_k : 1;
+  if (!encode_tile_map(&tk, k, Hkv, false, extent) || !encode_tile_map(&tv, v, Hkv, false, extent))
+    return BSA_ERR_INVALID_ARG;
+  Workspace *ws = nullptr;
+  if ((st = scratch_for(dev, stream, sizeof(Workspace), &ws)) != BSA_OK) return st;
+  const int rows = group * max_seqlen_q;
+  const bsa::DecLayout layout = bsa::DecLayout::make(n_seqs, Hq, Hkv, rows, total_k);
+  void *buf = nullptr;
+  if ((st = imp_scratch_for(dev, stream, layout.bytes, &buf, g_dec_scratch)) != BSA_OK) return st;
+  char *base = static_cast<char *>(buf);
+  bsa::DecParams p{};
+  p.dw = static_cast<bsa::DecWorkspace *>(buf);
+  p.ws = ws;
+  p.q = q;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.tile_off = reinterpret_cast<const int64_t *>(base + layout.tile_off);
+  p.item_off = reinterpret_cast<const int32_t *>(base + layout.item_off);
+  p.bm_off = reinterpret_cast<const int64_t *>(base + layout.bm_off);
+  p.S = reinterpret_cast<float *>(base + layout.S);
+  p.rm = reinterpret_cast<float *>(base + layout.rm);
+  p.skip = reinterpret_cast<uint8_t *>(base + layout.skip);
+  p.pO = reinterpret_cast<float *>(base + layout.pO);
+  p.pm = reinterpret_cast<float *>(base + layout.pm);
+  p.pl = reinterpret_cast<float *>(base + layout.pl);
+  p.out = out;
+  p.lse = lse;
+  p.bitmap = skip_bitmap;
+  p.total_k = total_k;
+  p.max_tiles = layout.max_tiles;
+  p.n_seqs = n_seqs;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.group = group;
+  p.rows = rows;
+  p.max_q = max_seqlen_q;
+  p.causal = causal;
+  p.c = (float)(1.0 / std::sqrt((double)d) * 1.4426950408889634);
+  p.log2_lambda = lambda > 0.f ? (float)std::log2((double)lambda) : -INFINITY;
+  p.wait_limit_ns = t_wait_limit_ns;
+  if (bsa::launch_decode(p, tk, tv, info->sm_count, stream) != cudaSuccess) return BSA_ERR_CUDA;
+  return BSA_OK;
 }
 
 int64_t bsa_importance_blocks(const int32_t *cu, int32_t n_seqs) {
@@ -453,6 +532,13 @@ void bsa_release(void) {
     }
   }
   g_imp_scratch.clear();
+  for (auto &kv : g_dec_scratch) {
+    if (kv.second.ptr) {
+      cudaSetDevice(kv.first.first);
+      cudaFree(kv.second.ptr);
+    }
+  }
+  g_dec_scratch.clear();
   cudaSetDevice(cur);
 }
 

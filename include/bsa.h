@@ -230,6 +230,37 @@ int64_t bsa_skip_bitmap_words_chunked(const int32_t *cu_seqlens_q_host,
                                       int32_t n_seqs, int32_t Hq);
 
 /*
+ * Decode with block skipping: a few new queries per sequence (the last Lq of
+ * its Lk positions, as bsa_prefill_fwd_chunked) against all its keys, with
+ * the key range split across the GPU. Same rule, decisions and outputs as
+ * bsa_prefill_fwd_chunked (the deployment guide applies the rule in decoding
+ * too, §6.1 suggesting lambda = 0.005 there).
+ *
+ * The split restates the order rule: a skipped tile never raises the running
+ * max (tile_max < m + ln(lambda) < m), so the running max before key tile j
+ * is the prefix max of the tile maxima before j, and tile j's decision follows
+ * from all tiles' maxima, computed first in parallel. Outputs are the online
+ * softmax over the kept tiles, merged across splits (P and the merge in fp32).
+ *
+ * q, k, v, cu_seqlens_q, cu_seqlens_k, n_seqs, Hq, Hkv, d, causal, lambda,
+ * out, lse, skip_bitmap: as bsa_prefill_fwd_chunked (bfloat16 only; the bitmap
+ * layout and size are those of bsa_skip_bitmap_words_chunked).
+ * max_seqlen_q  >= every Lq (checked on the device); (Hq / Hkv) * max_seqlen_q
+ *               <= 32 and Hq / Hkv <= 16.
+ * total_k       cu_seqlens_k[n_seqs], the rows of k and v (checked on the
+ *               device; a mismatch writes nothing, BSA_ERR_BAD_SEQLENS).
+ * Scratch (scores of the query rows for every key, per-split partial
+ * outputs) is library-owned, per stream, grown stream-ordered.
+ */
+bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
+                            const int32_t *cu_seqlens_q,
+                            const int32_t *cu_seqlens_k, int32_t n_seqs,
+                            int32_t max_seqlen_q, int64_t total_k, int32_t Hq,
+                            int32_t Hkv, int32_t d, int32_t causal,
+                            float lambda, void *out, float *lse,
+                            uint32_t *skip_bitmap, bsa_stream_t stream);
+
+/*
  * Token-block importance ("UniPrefill：通过分块动态稀疏化实现通用长上下文预填充
  * 加速", §3.2 Eq. (3)-(4)). For every sequence and query head h, the attention
  * weights A[j, i] of the last n = min(n_window, L) query positions j over

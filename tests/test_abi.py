@@ -133,6 +133,23 @@ def test_importance_argument_checks(L):
     assert call(d=64) == 2
 
 
+def test_decode_argument_checks(L):
+    a = dict(q=16, k=32, v=48, cq=64, ck=80, n=2, mq=1, tk=1000, Hq=32, Hkv=8, d=128, c=1,
+             lam=0.005, out=96, lse=None, bm=None)
+
+    def call(**o):
+        b = dict(a, **o)
+        return L.decode_fwd(b["q"], b["k"], b["v"], b["cq"], b["ck"], b["n"], b["mq"], b["tk"],
+                            b["Hq"], b["Hkv"], b["d"], b["c"], b["lam"], b["out"], b["lse"], b["bm"])
+    assert call(q=None) == 1 and call(v=None) == 1 and call(ck=None) == 1 and call(out=None) == 1
+    assert call(k=40) == 1 and call(cq=66) == 1 and call(lse=2) == 1
+    assert call(mq=0) == 1 and call(mq=9) == 1                # 4 x 9 rows > 32
+    assert call(Hq=32, Hkv=1) == 1                             # group above 16
+    assert call(tk=-1) == 1 and call(tk=1 << 31) == 1 and call(lam=1.0) == 1 and call(c=3) == 1
+    assert call(n=0) == 1 and call(Hq=30, Hkv=8) == 1
+    assert call(d=64) == 2
+
+
 def test_top_p_argument_checks(L):
     a = dict(sc=16, cu=32, n=1, tb=10, p=0.9, order=48, nsel=64, keep=None)
 

@@ -1,0 +1,112 @@
+"""GPU parity for the split-KV decode entry point (bsa_decode_fwd).
+
+Decode-shaped problems (a few queries per sequence, at the last positions,
+against all keys) are compared with the oracle's tile walk under the same
+tolerances as the prefill path: skip bits exact outside the 1e-3 decision
+margin, mask-replay outputs within max-abs 2e-2 / mean-abs 2e-3, lse within
+1e-3. The decisions of the split path come from prefix maxima of the tile
+maxima; the oracle walks the tiles in order, so the comparison also checks
+that restatement of the order rule.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import _cases
+import _gpu
+from gen import inputs as gi
+
+pytestmark = pytest.mark.gpu
+
+
+def run_decode(p, lam, causal=True, max_q=None, total_k=None, fill=float("nan")):
+    b = _gpu.bsa()
+    cuk = p.cu_seqlens_k
+    T = p.total_tokens
+    q, k, v = _gpu.to_dev_bf16(p.q), _gpu.to_dev_bf16(p.k), _gpu.to_dev_bf16(p.v)
+    cq = torch.from_numpy(p.cu_seqlens.astype(np.int32)).cuda()
+    ck = torch.from_numpy(cuk.astype(np.int32)).cuda()
+    max_q = int(p.seqlens.max()) if max_q is None else max_q
+    total_k = int(cuk[-1]) if total_k is None else total_k
+    out = torch.full((T, p.Hq, p.d), fill, dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((p.Hq, T), float("nan"), dtype=torch.float32, device="cuda")
+    nw = b.skip_bitmap_words_chunked(p.cu_seqlens, cuk, p.Hq)
+    bm = torch.full((max(nw, 1),), -1, dtype=torch.int32, device="cuda")
+    st = b.decode_fwd(q, k, v, cq, ck, p.n_seqs, max_q, total_k, p.Hq, p.Hkv, p.d, int(causal),
+                      lam, out, lse, bm)
+    b.check(st, "bsa_decode_fwd")
+    torch.cuda.synchronize()
+    status = b.get_device_status()
+    return dict(out=out, lse=lse, bitmap=bm[:nw].cpu().numpy().view(np.uint32), lam=lam,
+                causal=causal), status
+
+
+@pytest.fixture(scope="module")
+def g16():
+    # sixteen query heads on one KV head: the largest group the path takes
+    return gi.small("g16", [3000, 700], Hq=16, Hkv=1, seed=7)
+
+
+CASES = [("weak_sink", [1, 1]), ("gqa_ragged", [1, 3, 1, 2]), ("gqa4", [4, 1]),
+         ("tiny", [1, 2, 5]), ("no_sink", [1]), ("C0", [3])]
+
+
+@pytest.mark.parametrize("key,lq", CASES)
+@pytest.mark.parametrize("lam", [0.005, 0.0, 0.3])
+@pytest.mark.parametrize("causal", [True, False])
+def test_decode_matches_oracle(key, lq, lam, causal):
+    p = gi.chunk(_cases.small_problem(key), lq)
+    g, st = run_decode(p, lam, causal)
+    assert st == 0
+    out, lse = _gpu.host(g)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    print(key, lq, lam, causal, _gpu.compare(p, g))
+
+
+@pytest.mark.parametrize("lq", [[1, 1], [2, 1]])
+def test_decode_group_of_sixteen(g16, lq):
+    p = gi.chunk(g16, lq)
+    for lam in (0.005, 0.0):
+        g, st = run_decode(p, lam)
+        assert st == 0
+        _gpu.compare(p, g)
+
+
+def test_decode_max_seqlen_larger_than_needed():
+    # max_seqlen_q only bounds the rows; a loose bound gives the same result
+    p = gi.chunk(_cases.small_problem("gqa4"), [2, 1])
+    a, _ = run_decode(p, 0.005, max_q=2)
+    b, _ = run_decode(p, 0.005, max_q=8)
+    assert torch.equal(a["out"], b["out"]) and torch.equal(a["lse"], b["lse"])
+    assert np.array_equal(a["bitmap"], b["bitmap"])
+
+
+def test_decode_full_layer_one_query():
+    """One new query at the end of the 128K Llama-shaped layer, all 32 heads."""
+    p = gi.chunk(gi.config("C2"), [1])
+    for lam in (0.005, 0.0):
+        g, st = run_decode(p, lam)
+        assert st == 0
+        print(lam, _gpu.compare(p, g))
+
+
+def test_decode_batch_of_four_32k():
+    base = gi.packed("dec4", [32768] * 4, Hq=32, Hkv=8, seed=3, window=2.0, window_period=4096,
+                     window_len=512)
+    p = gi.chunk(base, [1, 2, 1, 1])
+    g, st = run_decode(p, 0.005)
+    assert st == 0
+    print(_gpu.compare(p, g))
+
+
+def test_decode_rejects_bad_lengths():
+    b = _gpu.bsa()
+    p = gi.chunk(_cases.small_problem("gqa4"), [4, 1])
+    # a query count above max_seqlen_q, then a wrong key total: nothing written
+    g, st = run_decode(p, 0.005, max_q=3, fill=7.0)
+    assert st == 6 and bool((g["out"] == 7.0).all())
+    g, st = run_decode(p, 0.005, total_k=int(p.cu_seqlens_k[-1]) - 1, fill=7.0)
+    assert st == 6 and bool((g["out"] == 7.0).all())
+    assert b.get_device_status() == 0
