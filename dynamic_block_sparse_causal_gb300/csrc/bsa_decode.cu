@@ -127,138 +127,215 @@ __global__ void __launch_bounds__(1024) dec_prologue_kernel(const __grid_constan
 
 // ============================================================ 1: scores
 
-// Warps 0-3: thread t = key t of the tile over the whole head dimension; it
-// copies its key row (16 x 16 bytes of the swizzled tile, conflict-free) to
-// registers and frees the stage at once, then takes the dot products with
-// the query rows (fp32, zero-padded to a multiple of four, read from shared
-// memory as warp-wide broadcasts), four rows at a time. Warp 4 lane 0 keeps
-// the K ring full across work items.
-__global__ void __launch_bounds__(kDecScoreThreads + 32, 2)
+// 32 lanes x 16 consecutive 32-bit TMEM columns; the wait is tied to the
+// destination registers.
+#define BSA_R8(i) "=r"(v[i]), "=r"(v[i + 1]), "=r"(v[i + 2]), "=r"(v[i + 3]), \
+                  "=r"(v[i + 4]), "=r"(v[i + 5]), "=r"(v[i + 6]), "=r"(v[i + 7])
+#define BSA_W8(i) "+r"(v[i]), "+r"(v[i + 1]), "+r"(v[i + 2]), "+r"(v[i + 3]), \
+                  "+r"(v[i + 4]), "+r"(v[i + 5]), "+r"(v[i + 6]), "+r"(v[i + 7])
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : BSA_R8(0), BSA_R8(8)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld16(uint32_t (&v)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : BSA_W8(0), BSA_W8(8) : : "memory");
+}
+#undef BSA_R8
+#undef BSA_W8
+
+// S^T = K Q^T on the tensor cores: M = 128 keys, N = the group's query rows
+// padded to 16 or 32, K = head dim. The contraction is tiny (the pass is
+// bound by reading K from DRAM) but it takes the dot products off the CUDA
+// cores and out of shared memory, whose bandwidth bounded the FMA version.
+//   warps 0-3  epilogue: TMEM lane = key; scales, masks and stores S, row maxima
+//   warp 4     lane 0: TMA producer of the K ring (all items of this CTA)
+//   warp 5     TMEM allocation; lane 0 issues the MMAs
+// The query rows of an item are written by the epilogue warps into one of two
+// 128-byte-swizzled K-major buffers (the MMA's B operand).
+template <int N>
+__global__ void __launch_bounds__(kDecScoreThreads + 64, 2)
 dec_scores_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensorMap tk) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ float red[2][kDecScoreThreads / 32][kDecMaxRows];
-  __shared__ uint64_t full[kStages], empty[kStages];
+  __shared__ uint64_t kfull[kStages], kempty[kStages], sfull[2], sempty[2], qready[2], qfree[2],
+      drain;
+  __shared__ uint32_t tmem_sh;
+  __shared__ volatile int abort_sh;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint32_t raw = smem_u32(smem_raw);
-  uint8_t *ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  float(*qs)[kTile] = reinterpret_cast<float(*)[kTile]>(ring + kStages * kTileBytes);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t *ring = smem_raw + (sbase - raw);
+  uint8_t *qbuf = ring + kStages * kTileBytes;   // two N x 256-byte buffers
+  constexpr uint32_t kQBytes = N * 256;
+  constexpr uint32_t kIdesc = IDesc<1, false, 128, N>::value;
+  constexpr int kEpi = kDecScoreThreads;
   if (t == 0) {
     for (int b = 0; b < kStages; ++b) {
-      mbar_init(&full[b], 1);
-      mbar_init(&empty[b], kDecScoreThreads / 32);
+      mbar_init(&kfull[b], 1);
+      mbar_init(&kempty[b], 1);
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sfull[b], 1);
+      mbar_init(&sempty[b], kEpi / 32);
+      mbar_init(&qready[b], 1);
+      mbar_init(&qfree[b], 1);
+    }
+    mbar_init(&drain, 1);
     fence_mbar_init();
+    abort_sh = 0;
   }
+  if (warp == 5) {
+    tmem_alloc(&tmem_sh, 2 * N < 32 ? 32 : 2 * N);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_sh;
   const int total = p.dw->total_items;
   const uint64_t limit = p.wait_limit_ns;
-  bool abort = false;
 
-  if (warp == kDecScoreThreads / 32) {
+  if (warp == 4) {
     // ---------------------------------------------------- TMA producer
     if (lane == 0) {
       uint32_t kc = 0;
       int last_issue[kStages] = {-1, -1, -1};
-      for (int item = blockIdx.x; item < total && !abort; item += gridDim.x) {
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok && !abort_sh; item += gridDim.x) {
         DecItem it;
         decode_item(p, item, it);
         for (int j = it.j0; j < it.j1; ++j, ++kc) {
           const uint32_t b = kc % kStages;
-          if (!mbar_wait(&empty[b], ((kc / kStages) & 1) ^ 1, limit)) {
-            abort = true;
-            break;
-          }
-          load_tile(ring + b * kTileBytes, &tk, &full[b], it.kvh, it.ak + j * kTile);
+          if (!(ok = mbar_wait(&kempty[b], ((kc / kStages) & 1) ^ 1, limit))) break;
+          load_tile(ring + b * kTileBytes, &tk, &kfull[b], it.kvh, it.ak + j * kTile);
           last_issue[b] = (int)kc;
         }
       }
-      if (abort)   // bounded wait for the copies still in flight
+      if (!ok) abort_sh = 1;
+      if (abort_sh)   // bounded wait for the copies still in flight
         for (int b = 0; b < kStages; ++b)
-          if (last_issue[b] >= 0) mbar_wait(&full[b], (last_issue[b] / kStages) & 1, limit);
+          if (last_issue[b] >= 0) mbar_wait(&kfull[b], (last_issue[b] / kStages) & 1, limit);
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t kc = 0, sc = 0, i = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok && !abort_sh; item += gridDim.x, ++i) {
+        DecItem it;
+        decode_item(p, item, it);
+        const uint32_t par = i & 1;
+        if (!(ok = mbar_wait(&qready[par], (i >> 1) & 1, limit))) break;
+        const uint32_t qs = sbase + kStages * kTileBytes + par * kQBytes;
+        for (int j = it.j0; j < it.j1; ++j, ++kc, ++sc) {
+          const uint32_t b = kc % kStages, buf = sc & 1;
+          if (!(ok = mbar_wait(&kfull[b], (kc / kStages) & 1, limit))) break;
+          if (!(ok = mbar_wait(&sempty[buf], ((sc >> 1) & 1) ^ 1, limit))) break;
+          tc_fence_after();
+          const uint32_t ks = sbase + b * kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t ka = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            const uint32_t kb = (kk >> 2) * (N * 128) + (kk & 3) * 32;
+            mma_f16_ss(tmem + buf * N, sdesc_sw128(ks + ka, 16, 1024), sdesc_sw128(qs + kb, 16, 1024),
+                       kIdesc, kk > 0);
+          }
+          mma_commit(&sfull[buf]);
+          mma_commit(&kempty[b]);
+        }
+        if (!ok) break;
+        mma_commit(&qfree[par]);
+      }
+      if (!ok) abort_sh = 1;
+      if (abort_sh) {   // this thread's MMAs finish before TMEM is freed
+        mma_commit(&drain);
+        mbar_wait(&drain, 0, limit);
+      }
     }
   } else {
-    // ---------------------------------------------------- consumers
+    // ---------------------------------------------------- epilogue
     const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
-    uint32_t kc = 0;
-    for (int item = blockIdx.x; item < total && !abort; item += gridDim.x) {
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    uint32_t sc = 0, i = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x, ++i) {
       DecItem it;
       decode_item(p, item, it);
-      const int R = p.group * it.Lq, Rpad = (R + 3) & ~3;
-      named_bar_sync(1, kDecScoreThreads);   // the previous item is done with qs
-      for (int r = 0; r < Rpad; ++r) {
-        float x = 0.f;
+      const int R = p.group * it.Lq;
+      const uint32_t par = i & 1;
+      // B operand: query row r at 128-byte-swizzled K-major position
+      // control flow below follows barrier reductions only, so the four
+      // warps always agree (abort_sh is also written by the other roles)
+      bool ok = i < 2 || mbar_wait(&qfree[par], ((i >> 1) - 1) & 1, limit);
+      if (bar_red_or(!ok, 1, kEpi)) {
+        abort_sh = 1;
+        break;
+      }
+      bool stop = false;
+      uint8_t *qb = qbuf + par * kQBytes;
+      for (int c = t; c < N * 16; c += kEpi) {
+        const int r = c >> 4, ch = c & 15;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
         if (r < R) {
           const int h = it.kvh * p.group + r / it.Lq, qi = r % it.Lq;
-          x = __bfloat162float(q[((size_t)(it.aq + qi) * p.Hq + h) * kTile + t]);
+          w = *reinterpret_cast<const uint4 *>(q + ((size_t)(it.aq + qi) * p.Hq + h) * kTile + ch * 8);
         }
-        qs[r][t] = x;
+        *reinterpret_cast<uint4 *>(qb + (ch >> 3) * (N * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = w;
       }
-      named_bar_sync(1, kDecScoreThreads);
+      fence_proxy_async_smem();
+      named_bar_sync(1, kEpi);
+      if (t == 0) mbar_arrive(&qready[par]);
       const int64_t toff = p.tile_off[it.s];
-      for (int j = it.j0; j < it.j1; ++j, ++kc) {
-        const uint32_t b = kc % kStages;
-        const bool ok = mbar_wait(&full[b], (kc / kStages) & 1, limit);
-        if (bar_red_or(!ok, 1, kDecScoreThreads)) {
-          abort = true;
+      for (int j = it.j0; j < it.j1; ++j, ++sc) {
+        const uint32_t buf = sc & 1;
+        ok = mbar_wait(&sfull[buf], (sc >> 1) & 1, limit);
+        if (bar_red_or(!ok, 1, kEpi)) {
+          abort_sh = 1;
+          stop = true;
           break;
         }
-        const uint8_t *kt = ring + b * kTileBytes;
-        uint4 kr[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) kr[c] = *reinterpret_cast<const uint4 *>(kt + swz(t, c));
+        tc_fence_after();
+        uint32_t v[N];
+        tmem_ld16(tmem + lane_off + buf * N, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+        if (N > 16) tmem_ld16(tmem + lane_off + buf * N + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[N > 16 ? 16 : 0]));
+        tmem_wait_ld16(*reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+        if (N > 16) tmem_wait_ld16(*reinterpret_cast<uint32_t(*)[16]>(&v[N > 16 ? 16 : 0]));
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[b]);
+        if (lane == 0) mbar_arrive(&sempty[buf]);
         const int kpos = j * kTile + t;
         const int64_t srow = ((toff + j) * p.Hkv + it.kvh) * p.rows;
         const int u = j - it.j0;
-        for (int rg = 0; rg < R; rg += 4) {
-          float acc[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float2 k0 = bf2(kr[c].x), k1 = bf2(kr[c].y), k2 = bf2(kr[c].z), k3 = bf2(kr[c].w);
+        for (int r = 0; r < N; ++r) {
+          if (r < R) {
+            const int pos = it.Lk - it.Lq + r % it.Lq;   // this query's key position
+            const bool masked = kpos >= it.Lk || (p.causal && kpos > pos);
+            const float s2 = masked ? -INFINITY : __uint_as_float(v[r]) * p.c;
+            p.S[(srow + r) * kTile + t] = s2;
+            float m = s2;
 #pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-              const float4 qa = *reinterpret_cast<const float4 *>(&qs[rg + rr][c * 8]);
-              const float4 qb = *reinterpret_cast<const float4 *>(&qs[rg + rr][c * 8 + 4]);
-              float x = acc[rr][c & 1];
-              x = fmaf(k0.x, qa.x, x);
-              x = fmaf(k0.y, qa.y, x);
-              x = fmaf(k1.x, qa.z, x);
-              x = fmaf(k1.y, qa.w, x);
-              x = fmaf(k2.x, qb.x, x);
-              x = fmaf(k2.y, qb.y, x);
-              x = fmaf(k3.x, qb.z, x);
-              x = fmaf(k3.y, qb.w, x);
-              acc[rr][c & 1] = x;
-            }
-          }
-#pragma unroll
-          for (int rr = 0; rr < 4; ++rr) {
-            const int r = rg + rr;
-            if (r < R) {
-              const int pos = it.Lk - it.Lq + r % it.Lq;   // this query's key position
-              const bool masked = kpos >= it.Lk || (p.causal && kpos > pos);
-              const float s2 = masked ? -INFINITY : (acc[rr][0] + acc[rr][1]) * p.c;
-              p.S[(srow + r) * kTile + t] = s2;
-              float m = s2;
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-              if (lane == 0) red[u & 1][warp][r] = m;
-            }
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) red[u & 1][warp][r] = m;
           }
         }
-        named_bar_sync(1, kDecScoreThreads);   // red[u & 1] complete
+        named_bar_sync(1, kEpi);   // red[u & 1] complete
         if (t < R) {
-          float m = red[u & 1][0][t];
-#pragma unroll
-          for (int w = 1; w < kDecScoreThreads / 32; ++w) m = fmaxf(m, red[u & 1][w][t]);
+          const float m = fmaxf(fmaxf(red[u & 1][0][t], red[u & 1][1][t]),
+                                fmaxf(red[u & 1][2][t], red[u & 1][3][t]));
           p.rm[(it.kvh * p.max_tiles + toff + j) * p.rows + t] = m;
         }
       }
+      if (stop) break;
     }
   }
+  tc_fence_before();
   __syncthreads();
-  if (abort && (t == 0 || t == kDecScoreThreads)) atomicOr(&p.ws->status, kStatusTimeout);
+  tc_fence_after();
+  if (abort_sh && t == 0) atomicOr(&p.ws->status, kStatusTimeout);
+  if (warp == 5) tmem_dealloc(tmem, 2 * N < 32 ? 32 : 2 * N);
 }
 
 // ============================================================ 2: decisions
@@ -593,7 +670,10 @@ cudaError_t launch_decode(const DecParams &p, const CUtensorMap &tk, const CUten
   const int64_t max_items = (int64_t)p.Hkv * (max_tiles / kDecSplit + p.n_seqs);
   const int grid = (int)(max_items < 8LL * sm_count ? max_items : 8LL * sm_count);
   dec_prologue_kernel<<<1, 1024, 0, stream>>>(p);
-  dec_scores_kernel<<<grid, kDecScoreThreads + 32, dec_smem_bytes(p.rows), stream>>>(p, tk);
+  if (p.rows <= 16)
+    dec_scores_kernel<16><<<grid, kDecScoreThreads + 64, dec_smem_bytes(16), stream>>>(p, tk);
+  else
+    dec_scores_kernel<32><<<grid, kDecScoreThreads + 64, dec_smem_bytes(32), stream>>>(p, tk);
   dec_decide_kernel<<<p.n_seqs * p.Hkv, 1024, 0, stream>>>(p);
   if (p.rows <= 4)
     dec_pv_kernel<4><<<grid, kDecThreads + 32, dec_smem_bytes(4), stream>>>(p, tv);
@@ -610,7 +690,9 @@ cudaError_t launch_decode(const DecParams &p, const CUtensorMap &tk, const CUten
 cudaError_t prepare_decode() {
   const int smem = (int)dec_smem_bytes(kDecMaxRows);
   cudaError_t e =
-      cudaFuncSetAttribute(dec_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaFuncSetAttribute(dec_scores_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(dec_scores_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(dec_pv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess)
