@@ -311,7 +311,6 @@ bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
   p.bm_off = reinterpret_cast<const int64_t *>(base + layout.bm_off);
   p.S = reinterpret_cast<float *>(base + layout.S);
   p.rm = reinterpret_cast<float *>(base + layout.rm);
-  p.skip = reinterpret_cast<uint8_t *>(base + layout.skip);
   p.pO = reinterpret_cast<float *>(base + layout.pO);
   p.pm = reinterpret_cast<float *>(base + layout.pm);
   p.pl = reinterpret_cast<float *>(base + layout.pl);

@@ -14,16 +14,17 @@
 //  1. dec_scores_kernel: for every (sequence, KV head, 16-tile split), the
 //     scaled scores S (log2 units) of the group's query rows against each key
 //     tile (TMA-staged, 3-stage ring) and their per-tile row maxima;
-//  2. dec_decide_kernel: per (sequence, KV head), a block-wide prefix-max scan
-//     over the tiles gives each tile's decision per query head (the AND over
-//     that head's rows) and the skip-bitmap words;
-//  3. dec_pv_kernel: per split, the kept tiles' V (TMA, only kept tiles) and
-//     an online softmax with the split's own reference max;
-//  4. dec_combine_kernel: merges the splits' (max, sum, output) per row.
+//  2. dec_pv_kernel: per split, the decisions (the prefix max of the earlier
+//     tiles' maxima, then the split's tiles in order; the AND over each query
+//     head's rows), the kept tiles' V (TMA, only kept tiles) and an online
+//     softmax with the split's own reference max;
+//  3. dec_combine_kernel: merges the splits' (max, sum, output) per row.
 // The decisions are exactly those of the sequential walk; outputs equal the
 // online softmax over the kept tiles up to rounding order. The work is
-// bandwidth-bound (K once, kept V once), so the dot products run on the
-// CUDA cores: one query row group of at most 32 rows per KV head.
+// bound by reading K once and the kept V once from DRAM; the two narrow
+// contractions (scores, P V) run on the tensor cores because the CUDA-core
+// versions were bound by shared-memory traffic, not by DRAM. One query row
+// group of at most 32 rows per KV head.
 #include <cuda_bf16.h>
 
 #include <climits>
@@ -68,11 +69,6 @@ __device__ __forceinline__ void decode_item(const DecParams &p, int item, DecIte
   (void)ns;
 }
 
-// Byte offset of 16-byte chunk c (0..15) of row r in a 128-byte-swizzled tile.
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-  return (uint32_t)((c >> 3) * kBoxBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
-
 __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, uint64_t *bar,
                                           int head, int row) {
   mbar_expect_tx(bar, kTileBytes);
@@ -80,8 +76,14 @@ __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, 
   tma_load_3d(dst + kBoxBytes, map, bar, 64, head, row);
 }
 
-__device__ __forceinline__ float2 bf2(uint32_t w) {
-  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+// Plain bulk copy global -> shared, completing on an mbarrier (16-byte
+// aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 }  // namespace
@@ -122,7 +124,13 @@ __global__ void __launch_bounds__(1024) dec_prologue_kernel(const __grid_constan
     if (items > INT_MAX) bad = true;
     p.dw->total_items = bad ? 0 : (int32_t)items;
     if (bad) atomicOr(&p.ws->status, kStatusBadSeqlens);
+    s_bad = bad;
   }
+  __syncthreads();
+  if (s_bad) return;
+  // the split passes OR their skip bits into the bitmap
+  if (p.bitmap)
+    for (int64_t w = tid; w < p.bm_off[p.n_seqs]; w += blockDim.x) p.bitmap[w] = 0u;
 }
 
 // ============================================================ 1: scores
@@ -338,246 +346,305 @@ dec_scores_kernel(const __grid_constant__ DecParams p, const __grid_constant__ C
   if (warp == 5) tmem_dealloc(tmem, 2 * N < 32 ? 32 : 2 * N);
 }
 
-// ============================================================ 2: decisions
+// ============================================================ 2: decide, P V
 
-// One CTA per (sequence, KV head); thread = key tile within a chunk of 1024.
-__global__ void __launch_bounds__(1024) dec_decide_kernel(const __grid_constant__ DecParams p) {
-  __shared__ float carry[kDecMaxRows];
-  __shared__ float wtot[32], wscan[32];
-  if (p.dw->total_items == 0) return;
-  const int s = blockIdx.x / p.Hkv, kvh = blockIdx.x - s * p.Hkv;
-  const int Lq = p.cu_q[s + 1] - p.cu_q[s], Lk = p.cu_k[s + 1] - p.cu_k[s];
-  if (Lq == 0) return;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int R = p.group * Lq, nk = (Lk + kTile - 1) / kTile, W = (nk + 31) / 32;
-  const int64_t toff = p.tile_off[s];
-  if (tid < R) carry[tid] = -INFINITY;
-  __syncthreads();
-  for (int base = 0; base < nk; base += 1024) {
-    const int j = base + tid;
-    const bool in = j < nk;
-    uint32_t skipb = (1u << p.group) - 1u;   // bit g: query head g of the group skips tile j
-    float xs[kDecMaxRows];
-    const float *rmj = p.rm + ((int64_t)kvh * p.max_tiles + toff + j) * p.rows;
-#pragma unroll
-    for (int r = 0; r < kDecMaxRows; ++r) xs[r] = (in && r < R) ? rmj[r] : -INFINITY;
-#pragma unroll
-    for (int r = 0; r < kDecMaxRows; ++r) {
-      if (r >= R) break;
-      const float x = xs[r];
-      float v = x;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v = fmaxf(v, y);
-      }
-      if (lane == 31) wtot[warp] = v;
-      __syncthreads();
-      if (warp == 0) {
-        float w = wtot[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, w, o);
-          if (lane >= o) w = fmaxf(w, y);
-        }
-        wscan[lane] = w;
-      }
-      __syncthreads();
-      float prev = __shfl_up_sync(0xffffffffu, v, 1);
-      if (lane == 0) prev = -INFINITY;
-      const float before = fmaxf(carry[r], fmaxf(warp > 0 ? wscan[warp - 1] : -INFINITY, prev));
-      // running max before tile j is the prefix max of the earlier tile maxima
-      if (!(x < before + p.log2_lambda)) skipb &= ~(1u << (r / Lq));
-      const float total = wscan[31];
-      __syncthreads();
-      if (tid == 0) carry[r] = fmaxf(carry[r], total);
-    }
-    if (in)
-      for (int g = 0; g < p.group; ++g)
-        p.skip[(toff + j) * p.Hq + kvh * p.group + g] = (uint8_t)((skipb >> g) & 1u);
-    if (p.bitmap) {
-      for (int g = 0; g < p.group; ++g) {
-        const uint32_t word = __ballot_sync(0xffffffffu, in && ((skipb >> g) & 1u));
-        const int w = (base >> 5) + warp;
-        if (lane == 0 && w < W)
-          p.bitmap[p.bm_off[s] + (int64_t)(kvh * p.group + g) * W + w] = word;
-      }
-    }
-    __syncthreads();
-  }
-}
-
-// ============================================================ 3: P V per split
-
-// Warps 0-7 (consumers). P: thread t computes key t%128 of the rows r with
-// r%2 == t/128. O: thread t accumulates columns 2(t%64), 2(t%64)+1 over keys
-// 32(t/64) .. +31, from its slice of the V tile copied to registers (which
-// frees the stage at once); the four key quarters are added at the end of
-// the split. Warp 8: the producer, which finds the kept tiles of each split
-// with one ballot and keeps the V ring full across work items.
-// RB >= group x Lq rows.
+// One work item = (sequence, KV head, 16-tile split), as in the score pass.
+//   warps 0-3  decisions of the split: the row maxima of all earlier tiles
+//              (prefix max), then a walk over the split's tiles; skip bits go
+//              to the bitmap (OR into words the prologue zeroed). Then per
+//              kept tile: P (thread t = key t, fp32 exponentials and row sums)
+//              into a 128-byte-swizzled bf16 buffer, and O = alpha O + D
+//              (thread t = head-dim column t, D read from TMEM).
+//   warp 4     V producer for the kept tiles
+//   warp 5     TMEM allocation; lane 0 issues O^T = V^T P^T per kept tile:
+//              A = the V tile read MN-major (M = head dim), B = P (the
+//              group's rows padded to N, keys contiguous), D in one of two
+//              TMEM buffers.
+// RB >= group x Lq rows; N = RB rounded up to 16.
 template <int RB>
-__global__ void __launch_bounds__(kDecThreads + 32, RB <= 8 ? 2 : 1)
+__global__ void __launch_bounds__(kDecScoreThreads + 64, RB <= 16 ? 2 : 1)
 dec_pv_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensorMap tv) {
+  constexpr int N = RB < 16 ? 16 : RB;
+  constexpr int kEpi = kDecScoreThreads;
+  constexpr uint32_t kPBytes = N * 256;
+  // ring stage: the V tile, then the kept tile's scores S (rows x 128 fp32)
+  constexpr uint32_t kStage = kTileBytes + RB * kTile * 4;
+  // bf16 x bf16 -> f32, A MN-major (bit 15), B K-major, M = 128, N
+  constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) |
+                              ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
   extern __shared__ uint8_t smem_raw[];
-  __shared__ float lred[kDecThreads / 32][RB];
-  __shared__ uint64_t full[kStages], empty[kStages];
-  __shared__ int klist[kDecSplit];
-  __shared__ uint32_t kact[kDecSplit], kact_raw[kDecSplit];
-  __shared__ int nkept_sh;
+  __shared__ float lred[kEpi / 32][RB];
+  __shared__ float mred[kEpi / 32][RB];
+  __shared__ float srm[kDecSplit * RB];
+  __shared__ uint32_t predmask[RB];
+  __shared__ uint64_t vfull[kStages], vempty[kStages], pready[2], pfree[2], dfull[2], dempty[2],
+      lready[2], lfree[2], drain;
+  __shared__ int klist[2][kDecSplit];
+  __shared__ uint32_t kact[2][kDecSplit];
+  __shared__ int nkept_sh[2];
+  __shared__ uint32_t tmem_sh;
+  __shared__ volatile int abort_sh;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint32_t raw = smem_u32(smem_raw);
-  uint8_t *ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  float(*ps)[kTile] = reinterpret_cast<float(*)[kTile]>(ring + kStages * kTileBytes);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t *ring = smem_raw + (sbase - raw);
+  uint8_t *pbuf = ring + kStages * kStage;
   if (t == 0) {
     for (int b = 0; b < kStages; ++b) {
-      mbar_init(&full[b], 1);
-      mbar_init(&empty[b], kDecThreads / 32);
+      mbar_init(&vfull[b], 1);
+      mbar_init(&vempty[b], 2);   // the MMA has read V, the epilogue has read S
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&pready[b], 1);
+      mbar_init(&pfree[b], 1);
+      mbar_init(&dfull[b], 1);
+      mbar_init(&dempty[b], kEpi / 32);
+      mbar_init(&lready[b], 1);
+      mbar_init(&lfree[b], 2);
+    }
+    mbar_init(&drain, 1);
     fence_mbar_init();
+    abort_sh = 0;
   }
+  if (warp == 5) {
+    tmem_alloc(&tmem_sh, 2 * N < 32 ? 32 : 2 * N);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_sh;
   const int total = p.dw->total_items;
   const uint64_t limit = p.wait_limit_ns;
-  bool abort = false;
 
-  if (warp == kDecThreads / 32) {
+  if (warp == 4) {
     // ---------------------------------------------------- V producer
-    uint32_t vc = 0;
-    int last_issue[kStages] = {-1, -1, -1};
-    for (int item = blockIdx.x; item < total && !abort; item += gridDim.x) {
-      DecItem it;
-      decode_item(p, item, it);
-      const int64_t toff = p.tile_off[it.s];
-      bool kept_l = false;   // lane l: tile j0 + l kept by some head of the group
-      if (lane < it.j1 - it.j0)
-        for (int g = 0; g < p.group; ++g)
-          kept_l |= !p.skip[(toff + it.j0 + lane) * p.Hq + it.kvh * p.group + g];
-      uint32_t kept = __ballot_sync(0xffffffffu, kept_l);
-      if (lane == 0) {
-        while (kept) {
-          const int l = __ffs(kept) - 1;
-          kept &= kept - 1;
-          const uint32_t b = vc % kStages;
-          if (!mbar_wait(&empty[b], ((vc / kStages) & 1) ^ 1, limit)) {
-            abort = true;
+    if (lane == 0) {
+      uint32_t kc = 0, i = 0;
+      int last_issue[kStages] = {-1, -1, -1};
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++i) {
+        DecItem it;
+        decode_item(p, item, it);
+        const uint32_t par = i & 1;
+        if (!(ok = mbar_wait(&lready[par], (i >> 1) & 1, limit))) break;
+        const int n = nkept_sh[par];
+        const int R = p.group * it.Lq;
+        const int64_t toff = p.tile_off[it.s];
+        for (int u = 0; u < n; ++u) {
+          const uint32_t b = kc % kStages;
+          if (!(ok = mbar_wait(&vempty[b], ((kc / kStages) & 1) ^ 1, limit)) || abort_sh) {
+            ok = false;
             break;
           }
-          load_tile(ring + b * kTileBytes, &tv, &full[b], it.kvh, it.ak + (it.j0 + l) * kTile);
-          last_issue[b] = (int)vc++;
+          const int j = klist[par][u];
+          uint8_t *st = ring + b * kStage;
+          mbar_expect_tx(&vfull[b], kTileBytes + R * kTile * 4);
+          tma_load_3d(st, &tv, &vfull[b], 0, it.kvh, it.ak + j * kTile);
+          tma_load_3d(st + kBoxBytes, &tv, &vfull[b], 64, it.kvh, it.ak + j * kTile);
+          bulk_load(st + kTileBytes, p.S + ((toff + j) * p.Hkv + it.kvh) * p.rows * kTile,
+                    R * kTile * 4, &vfull[b]);
+          last_issue[b] = (int)kc++;
+        }
+        mbar_arrive(&lfree[par]);
+      }
+      if (!ok) {
+        abort_sh = 1;
+        for (int b = 0; b < kStages; ++b)
+          if (last_issue[b] >= 0) mbar_wait(&vfull[b], (last_issue[b] / kStages) & 1, limit);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t kc = 0, i = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++i) {
+        const uint32_t par = i & 1;
+        if (!(ok = mbar_wait(&lready[par], (i >> 1) & 1, limit))) break;
+        const int n = nkept_sh[par];
+        mbar_arrive(&lfree[par]);
+        for (int u = 0; u < n; ++u, ++kc) {
+          const uint32_t b = kc % kStages, slot = kc & 1;
+          if (!(ok = mbar_wait(&vfull[b], (kc / kStages) & 1, limit))) break;
+          if (!(ok = mbar_wait(&pready[slot], (kc >> 1) & 1, limit))) break;
+          if (!(ok = mbar_wait(&dempty[slot], ((kc >> 1) & 1) ^ 1, limit))) break;
+          if (abort_sh) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t vs = sbase + b * kStage;
+          const uint32_t ps = sbase + kStages * kStage + slot * kPBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            // A: 16 keys = two 8-key swizzle atoms (2048 bytes); the two 64-wide
+            // halves of the head dim are one box apart. B: 32 bytes per K step.
+            const uint64_t ad = sdesc_sw128(vs + kk * 2048, kBoxBytes, 1024);
+            const uint64_t bd = sdesc_sw128(ps + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
+            mma_f16_ss(tmem + slot * N, ad, bd, kIdesc, kk > 0);
+          }
+          mma_commit(&dfull[slot]);
+          mma_commit(&vempty[b]);
+          mma_commit(&pfree[slot]);
         }
       }
-      abort = __shfl_sync(0xffffffffu, abort, 0);
+      if (!ok) {
+        abort_sh = 1;
+        mma_commit(&drain);
+        mbar_wait(&drain, 0, limit);
+      }
     }
-    if (abort && lane == 0)
-      for (int b = 0; b < kStages; ++b)
-        if (last_issue[b] >= 0) mbar_wait(&full[b], (last_issue[b] / kStages) & 1, limit);
   } else {
-    // ---------------------------------------------------- consumers
-    const int cp = t & 63, kq = t >> 6, pk = t & (kTile - 1), prow = t >> 7;
-    const int col = 2 * cp;
-    uint32_t vc = 0;
-    for (int item = blockIdx.x; item < total && !abort; item += gridDim.x) {
+    // ---------------------------------------------------- epilogue
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    uint32_t kc = 0, i = 0;
+    bool stop = false;
+    for (int item = blockIdx.x; item < total && !stop; item += gridDim.x, ++i) {
       DecItem it;
       decode_item(p, item, it);
-      const int R = p.group * it.Lq;
+      const int R = p.group * it.Lq, nt = it.j1 - it.j0;
       const int64_t toff = p.tile_off[it.s];
-      named_bar_sync(1, kDecThreads);   // the previous item is done with klist and ps
-      if (t < kDecSplit) kact_raw[t] = 0;
-      named_bar_sync(1, kDecThreads);
-      {
-        const int u = t / p.group, g = t - u * p.group;
-        if (u < it.j1 - it.j0 && !p.skip[(toff + it.j0 + u) * p.Hq + it.kvh * p.group + g])
-          atomicOr(&kact_raw[u], 1u << g);
+      const uint32_t par = i & 1;
+      const float *rmh = p.rm + ((int64_t)it.kvh * p.max_tiles + toff) * p.rows;
+      // ---- decisions. Running max before the split: the max of the earlier
+      // tiles' row maxima. Rp (R rounded up to a power of two) divides the
+      // thread stride, so thread t always meets row t % Rp; the split's own
+      // maxima go to shared memory for the walk in order.
+      const int Rp = R <= 1 ? 1 : 1 << (32 - __clz(R - 1));
+      const int rt = t & (Rp - 1);
+      float mp = -INFINITY;
+      if (rt < R) {
+#pragma unroll 8
+        for (int idx = t; idx < it.j0 * Rp; idx += kEpi)
+          mp = fmaxf(mp, rmh[(int64_t)(idx / Rp) * p.rows + rt]);
       }
-      named_bar_sync(1, kDecThreads);
+      for (int idx = t; idx < nt * R; idx += kEpi)
+        srm[idx] = rmh[(int64_t)(it.j0 + idx / R) * p.rows + idx % R];
+      for (int o = 16; o >= Rp; o >>= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
+      if (lane < Rp) mred[warp][lane] = mp;
+      // the lists of item i - 2 are no longer read by the producer and MMA
+      const bool okl = i < 2 || mbar_wait(&lfree[par], ((i >> 1) - 1) & 1, limit);
+      if (bar_red_or(!okl, 1, kEpi)) {
+        stop = true;
+        break;
+      }
+      if (t < R) {   // walk the split's tiles in order, per row
+        float mr = fmaxf(fmaxf(mred[0][t], mred[1][t]), fmaxf(mred[2][t], mred[3][t]));
+        uint32_t bits = 0;   // bit u: row t would skip tile j0 + u
+        for (int u = 0; u < nt; ++u) {
+          const float x = srm[u * R + t];
+          if (x < mr + p.log2_lambda) bits |= 1u << u;
+          mr = fmaxf(mr, x);
+        }
+        predmask[t] = bits;
+      }
+      named_bar_sync(1, kEpi);
       if (t == 0) {
         int n = 0;
-        for (int u = 0; u < it.j1 - it.j0; ++u)
-          if (kact_raw[u]) {
-            klist[n] = it.j0 + u;
-            kact[n] = kact_raw[u];
+        for (int u = 0; u < nt; ++u) {
+          uint32_t act = 0;   // heads of the group that keep tile j0 + u
+          for (int g = 0; g < p.group; ++g) {
+            bool keep = false;
+            for (int qi = 0; qi < it.Lq; ++qi) keep |= !((predmask[g * it.Lq + qi] >> u) & 1u);
+            if (keep) act |= 1u << g;
+          }
+          if (act) {
+            klist[par][n] = it.j0 + u;
+            kact[par][n] = act;
             ++n;
           }
-        nkept_sh = n;
+        }
+        nkept_sh[par] = n;
+        mbar_arrive(&lready[par]);
       }
-      named_bar_sync(1, kDecThreads);
-      const int n = nkept_sh;
-      float O[RB][2], mref[RB], lsum[RB];
+      if (p.bitmap && t < p.group) {   // this split's 16 bits of each head's row
+        uint32_t bits = 0xFFFFu;
+        for (int qi = 0; qi < it.Lq; ++qi) bits &= predmask[t * it.Lq + qi];
+        bits &= (nt >= 32 ? 0xFFFFFFFFu : ((1u << nt) - 1u));
+        const int nk = (it.Lk + kTile - 1) / kTile, W = (nk + 31) / 32;
+        if (bits)
+          atomicOr(p.bitmap + p.bm_off[it.s] + (int64_t)(it.kvh * p.group + t) * W + (it.j0 >> 5),
+                   bits << (it.j0 & 31));
+      }
+      named_bar_sync(1, kEpi);
+      const int n = nkept_sh[par];
+      // ---- kept tiles
+      float O[RB], mref[RB], lsum[RB], alpha[RB], alpha_prev[RB];
 #pragma unroll
       for (int r = 0; r < RB; ++r) {
-        O[r][0] = O[r][1] = 0.f;
+        O[r] = 0.f;
         mref[r] = -INFINITY;
         lsum[r] = 0.f;
+        alpha[r] = alpha_prev[r] = 1.f;
       }
-      for (int u = 0; u < n; ++u, ++vc) {
-        const int j = klist[u];
-        const uint32_t act = kact[u];
-        const int64_t srow = ((toff + j) * p.Hkv + it.kvh) * p.rows;
-        const float *rmj = p.rm + ((int64_t)it.kvh * p.max_tiles + toff + j) * p.rows;
-        float alpha[RB];
+      // O += D of kept tile number kd (its P used the reference alpha_prev)
+      auto take_d = [&](uint32_t kd) -> bool {
+        const uint32_t slot = kd & 1;
+        const bool okd = mbar_wait(&dfull[slot], (kd >> 1) & 1, limit);
+        if (bar_red_or(!okd, 1, kEpi)) return false;
+        tc_fence_after();
+        uint32_t v[N];
 #pragma unroll
-        for (int r = 0; r < RB; ++r) {
-          alpha[r] = 1.f;
-          if (r < R) {
+        for (int h = 0; h < N / 16; ++h)
+          tmem_ld16(tmem + lane_off + slot * N + h * 16, *reinterpret_cast<uint32_t(*)[16]>(&v[h * 16]));
+#pragma unroll
+        for (int h = 0; h < N / 16; ++h) tmem_wait_ld16(*reinterpret_cast<uint32_t(*)[16]>(&v[h * 16]));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dempty[slot]);
+#pragma unroll
+        for (int r = 0; r < RB; ++r) O[r] = fmaf(O[r], alpha_prev[r], __uint_as_float(v[r]));
+        return true;
+      };
+      for (int u = 0; u < n && !stop; ++u, ++kc) {
+        const int j = klist[par][u];
+        const uint32_t act = kact[par][u], slot = kc & 1, b = kc % kStages;
+        const float *rmj = rmh + (int64_t)j * p.rows;
+        // P buffer slot free (the MMA two kept tiles back has read it), and
+        // this tile's V and S landed
+        const bool okp = mbar_wait(&pfree[slot], ((kc >> 1) & 1) ^ 1, limit) &&
+                         mbar_wait(&vfull[b], (kc / kStages) & 1, limit);
+        if (bar_red_or(!okp, 1, kEpi)) {
+          stop = true;
+          break;
+        }
+        const float *Ss = reinterpret_cast<const float *>(ring + b * kStage + kTileBytes);
+        uint8_t *pb = pbuf + slot * kPBytes;
+#pragma unroll
+        for (int r = 0; r < N; ++r) {
+          float pv = 0.f;
+          if (r < RB && r < R) {
             const bool on = (act >> (r / it.Lq)) & 1u;
             const float mnew = on ? fmaxf(mref[r], rmj[r]) : mref[r];
             alpha[r] = mnew == -INFINITY ? 1.f : ex2_approx(mref[r] - mnew);
             mref[r] = mnew;
-            if ((r & 1) == prow) {
-              const float pv =
-                  (on && mnew != -INFINITY) ? ex2_approx(p.S[(srow + r) * kTile + pk] - mnew) : 0.f;
-              ps[r][pk] = pv;
-              lsum[r] = lsum[r] * alpha[r] + pv;
-            }
+            pv = (on && mnew != -INFINITY) ? ex2_approx(Ss[r * kTile + t] - mnew) : 0.f;
+            lsum[r] = fmaf(lsum[r], alpha[r], pv);
+          } else if (r < RB) {
+            alpha[r] = 1.f;
           }
+          // key t of row r: box t/64, 16-byte chunk (t%64)/8 swizzled by row
+          *reinterpret_cast<__nv_bfloat16 *>(pb + (t >> 6) * (N * 128) + r * 128 +
+                                             ((((t >> 3) & 7) ^ (r & 7)) << 4) + (t & 7) * 2) =
+              __float2bfloat16_rn(pv);
         }
-        const uint32_t b = vc % kStages;
-        const bool ok = mbar_wait(&full[b], (vc / kStages) & 1, limit);
-        if (bar_red_or(!ok, 1, kDecThreads)) {   // also publishes ps
-          abort = true;
+        fence_proxy_async_smem();
+        named_bar_sync(1, kEpi);
+        if (t == 0) {
+          mbar_arrive(&pready[slot]);
+          mbar_arrive(&vempty[b]);   // S of this stage has been read
+        }
+        if (u > 0 && !take_d(kc - 1)) {
+          stop = true;
           break;
         }
-        const uint8_t *vt = ring + b * kTileBytes;
-        uint32_t vr[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          vr[e] = *reinterpret_cast<const uint32_t *>(vt + swz(kq * 32 + e, col >> 3) + (col & 7) * 2);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[b]);
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-          O[r][0] *= alpha[r];
-          O[r][1] *= alpha[r];
-        }
-#pragma unroll
-        for (int k4 = 0; k4 < 8; ++k4) {
-          const float2 v0 = bf2(vr[4 * k4]), v1 = bf2(vr[4 * k4 + 1]);
-          const float2 v2 = bf2(vr[4 * k4 + 2]), v3 = bf2(vr[4 * k4 + 3]);
-#pragma unroll
-          for (int r = 0; r < RB; ++r) {
-            if (r < R) {
-              const float4 pr = *reinterpret_cast<const float4 *>(&ps[r][kq * 32 + 4 * k4]);
-              O[r][0] = fmaf(pr.x, v0.x, fmaf(pr.y, v1.x, fmaf(pr.z, v2.x, fmaf(pr.w, v3.x, O[r][0]))));
-              O[r][1] = fmaf(pr.x, v0.y, fmaf(pr.y, v1.y, fmaf(pr.z, v2.y, fmaf(pr.w, v3.y, O[r][1]))));
-            }
-          }
-        }
-        named_bar_sync(1, kDecThreads);   // ps is free again
+        for (int r = 0; r < RB; ++r) alpha_prev[r] = alpha[r];
       }
-      if (abort) break;
-      // the four key quarters of O meet in ps; the row sums in lred
-      for (int qq = 3; qq >= 0; --qq) {
-        if (kq == qq)
-#pragma unroll
-          for (int r = 0; r < RB; ++r)
-            if (r < R) {
-              const float a0 = qq == 3 ? 0.f : ps[r][col], a1 = qq == 3 ? 0.f : ps[r][col + 1];
-              ps[r][col] = a0 + O[r][0];
-              ps[r][col + 1] = a1 + O[r][1];
-            }
-        named_bar_sync(1, kDecThreads);
-      }
+      if (!stop && n > 0 && !take_d(kc - 1)) stop = true;
+      if (stop) break;
+      // ---- write the split: O (thread t = column), the row sums, the reference max
 #pragma unroll
       for (int r = 0; r < RB; ++r) {
         float x = lsum[r];
@@ -585,29 +652,31 @@ dec_pv_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUten
         for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
         if (lane == 0) lred[warp][r] = x;
       }
-      named_bar_sync(1, kDecThreads);
-      const int64_t prow_off = (int64_t)item * p.rows;
-      for (int i = t; i < R * kTile; i += kDecThreads)
-        p.pO[prow_off * kTile + i] = ps[i >> 7][i & (kTile - 1)];
-      if (t < R) {
-        float l = 0.f;
+      named_bar_sync(1, kEpi);
+      const int64_t prow = (int64_t)item * p.rows;
 #pragma unroll
-        for (int w = 0; w < kDecThreads / 32; ++w) l += lred[w][t];
-        p.pl[prow_off + t] = l;
+      for (int r = 0; r < RB; ++r)
+        if (r < R) p.pO[(prow + r) * kTile + t] = O[r];
+      if (t < R) {
+        p.pl[prow + t] = (lred[0][t] + lred[1][t]) + (lred[2][t] + lred[3][t]);
 #pragma unroll
         for (int r = 0; r < RB; ++r)
-          if (r == t) p.pm[prow_off + t] = mref[r];
+          if (r == t) p.pm[prow + t] = mref[r];
       }
     }
+    if (stop) abort_sh = 1;
   }
+  tc_fence_before();
   __syncthreads();
-  if (abort && (t == 0 || t == kDecThreads)) atomicOr(&p.ws->status, kStatusTimeout);
+  tc_fence_after();
+  if (abort_sh && t == 0) atomicOr(&p.ws->status, kStatusTimeout);
+  if (warp == 5) tmem_dealloc(tmem, 2 * N < 32 ? 32 : 2 * N);
 }
 
-// ============================================================ 4: merge
+// ============================================================ 3: merge
 
 // One CTA per (sequence, query slot, query head); thread t = column t%128 of
-// the splits i with i%4 == t/128, the four groups added at the end.
+// the splits q with q%4 == t/128, the four groups added at the end.
 __global__ void __launch_bounds__(4 * kTile) dec_combine_kernel(const __grid_constant__ DecParams p) {
   __shared__ float red[4 * kTile / 32];
   __shared__ float part[3][kTile], lpart[4];
@@ -621,10 +690,10 @@ __global__ void __launch_bounds__(4 * kTile) dec_combine_kernel(const __grid_con
   const int Lk = p.cu_k[s + 1] - p.cu_k[s];
   const int nk = (Lk + kTile - 1) / kTile, ns = (nk + kDecSplit - 1) / kDecSplit;
   const int kvh = h / p.group, r = (h - kvh * p.group) * Lq + qi;
-  const int64_t it0 = (int64_t)p.item_off[s] + kvh;   // split i is item it0 + i * Hkv
+  const int64_t it0 = (int64_t)p.item_off[s] + kvh;   // split q is item it0 + q * Hkv
   const int64_t H = p.Hkv;
   float m = -INFINITY;
-  for (int i = t; i < ns; i += 4 * kTile) m = fmaxf(m, p.pm[(it0 + i * H) * p.rows + r]);
+  for (int q = t; q < ns; q += 4 * kTile) m = fmaxf(m, p.pm[(it0 + q * H) * p.rows + r]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if (lane == 0) red[warp] = m;
@@ -634,8 +703,8 @@ __global__ void __launch_bounds__(4 * kTile) dec_combine_kernel(const __grid_con
   for (int w = 1; w < 4 * kTile / 32; ++w) m = fmaxf(m, red[w]);
   float acc = 0.f, l = 0.f;
 #pragma unroll 4
-  for (int i = grp; i < ns; i += 4) {
-    const int64_t ii = it0 + i * H;
+  for (int q = grp; q < ns; q += 4) {
+    const int64_t ii = it0 + q * H;
     const float mi = p.pm[ii * p.rows + r];
     if (mi == -INFINITY) continue;   // no kept tile of this split for the row
     const float w = ex2_approx(mi - m);
@@ -662,6 +731,11 @@ namespace {
 size_t dec_smem_bytes(int rows) {
   return (size_t)kStages * kTileBytes + 1024 + (size_t)((rows + 3) & ~3) * kTile * 4;
 }
+// V ring with the staged scores, then two P buffers (N = RB rounded up to 16)
+size_t pv_smem_bytes(int RB) {
+  const int N = RB < 16 ? 16 : RB;
+  return (size_t)kStages * (kTileBytes + RB * kTile * 4) + 1024 + 2 * (size_t)N * 256;
+}
 }  // namespace
 
 cudaError_t launch_decode(const DecParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
@@ -674,15 +748,14 @@ cudaError_t launch_decode(const DecParams &p, const CUtensorMap &tk, const CUten
     dec_scores_kernel<16><<<grid, kDecScoreThreads + 64, dec_smem_bytes(16), stream>>>(p, tk);
   else
     dec_scores_kernel<32><<<grid, kDecScoreThreads + 64, dec_smem_bytes(32), stream>>>(p, tk);
-  dec_decide_kernel<<<p.n_seqs * p.Hkv, 1024, 0, stream>>>(p);
   if (p.rows <= 4)
-    dec_pv_kernel<4><<<grid, kDecThreads + 32, dec_smem_bytes(4), stream>>>(p, tv);
+    dec_pv_kernel<4><<<grid, kDecScoreThreads + 64, pv_smem_bytes(4), stream>>>(p, tv);
   else if (p.rows <= 8)
-    dec_pv_kernel<8><<<grid, kDecThreads + 32, dec_smem_bytes(8), stream>>>(p, tv);
+    dec_pv_kernel<8><<<grid, kDecScoreThreads + 64, pv_smem_bytes(8), stream>>>(p, tv);
   else if (p.rows <= 16)
-    dec_pv_kernel<16><<<grid, kDecThreads + 32, dec_smem_bytes(16), stream>>>(p, tv);
+    dec_pv_kernel<16><<<grid, kDecScoreThreads + 64, pv_smem_bytes(16), stream>>>(p, tv);
   else
-    dec_pv_kernel<32><<<grid, kDecThreads + 32, dec_smem_bytes(32), stream>>>(p, tv);
+    dec_pv_kernel<32><<<grid, kDecScoreThreads + 64, pv_smem_bytes(32), stream>>>(p, tv);
   dec_combine_kernel<<<p.n_seqs * p.max_q * p.Hq, 4 * kTile, 0, stream>>>(p);
   return cudaGetLastError();
 }
@@ -694,13 +767,17 @@ cudaError_t prepare_decode() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(dec_scores_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(dec_pv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(dec_pv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)pv_smem_bytes(4));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(dec_pv_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(dec_pv_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)pv_smem_bytes(8));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(dec_pv_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(dec_pv_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)pv_smem_bytes(16));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(dec_pv_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(dec_pv_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)pv_smem_bytes(32));
   return e;
 }
 

@@ -21,7 +21,6 @@ constexpr int kDecScoreThreads = 128;  // score pass: one thread per key of a ti
 //   int64 bm_off[n_seqs + 1]     first skip-bitmap word of every sequence
 //   float S[tiles][Hkv][rows][128]  scaled scores (log2 units), -inf where masked
 //   float rm[Hkv][tiles][rows]      their row maxima per tile
-//   uint8 skip[tiles][Hq]           1 = key tile skipped for that query head
 //   float pO[items][rows][128], pm[items][rows], pl[items][rows]
 //                                   per-split output, reference max, sum
 // with tiles <= total_k / 128 + n_seqs and items <= Hkv (tiles / 16 + n_seqs).
@@ -31,7 +30,7 @@ struct alignas(128) DecWorkspace {
 };
 
 struct DecLayout {
-  size_t tile_off, item_off, bm_off, S, rm, skip, pO, pm, pl, bytes;
+  size_t tile_off, item_off, bm_off, S, rm, pO, pm, pl, bytes;
   int64_t max_tiles, max_items;
   static DecLayout make(int n_seqs, int Hq, int Hkv, int rows, int64_t total_k) {
     DecLayout l;
@@ -49,8 +48,6 @@ struct DecLayout {
     off += up((size_t)l.max_tiles * Hkv * rows * kTile * 4);
     l.rm = off;
     off += up((size_t)l.max_tiles * Hkv * rows * 4);
-    l.skip = off;
-    off += up((size_t)l.max_tiles * Hq);
     l.pO = off;
     off += up((size_t)l.max_items * rows * kTile * 4);
     l.pm = off;
@@ -70,7 +67,6 @@ struct DecParams {
   const int64_t *tile_off, *bm_off;
   const int32_t *item_off;
   float *S, *rm, *pO, *pm, *pl;
-  uint8_t *skip;
   void *out;                  // bf16 [total_q, Hq, 128]
   float *lse;                 // [Hq, total_q] or null
   uint32_t *bitmap;           // or null
