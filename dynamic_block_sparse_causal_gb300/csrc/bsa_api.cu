@@ -296,7 +296,9 @@ bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
   Workspace *ws = nullptr;
   if ((st = scratch_for(dev, stream, sizeof(Workspace), &ws)) != BSA_OK) return st;
   const int rows = group * max_seqlen_q;
-  const bsa::DecLayout layout = bsa::DecLayout::make(n_seqs, Hq, Hkv, rows, total_k);
+  // 16-tile splits unless that leaves fewer than four work items per SM
+  const int split = (int64_t)Hkv * (total_k / bsa::kTile) / 16 < 4LL * info->sm_count ? 8 : 16;
+  const bsa::DecLayout layout = bsa::DecLayout::make(n_seqs, Hq, Hkv, rows, total_k, split);
   void *buf = nullptr;
   if ((st = imp_scratch_for(dev, stream, layout.bytes, &buf, g_dec_scratch)) != BSA_OK) return st;
   char *base = static_cast<char *>(buf);
@@ -325,6 +327,7 @@ bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
   p.group = group;
   p.rows = rows;
   p.max_q = max_seqlen_q;
+  p.split = split;
   p.causal = causal;
   p.c = (float)(1.0 / std::sqrt((double)d) * 1.4426950408889634);
   p.log2_lambda = lambda > 0.f ? (float)std::log2((double)lambda) : -INFINITY;

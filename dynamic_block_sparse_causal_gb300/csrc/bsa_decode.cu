@@ -58,15 +58,13 @@ __device__ __forceinline__ void decode_item(const DecParams &p, int item, DecIte
   it.ak = p.cu_k[lo];
   it.Lk = p.cu_k[lo + 1] - it.ak;
   const int nk = (it.Lk + kTile - 1) / kTile;
-  const int ns = (nk + kDecSplit - 1) / kDecSplit;
   // the KV heads of one split are neighbours: CTAs running together read
   // whole token rows of K and V (all heads) from DRAM
   const int local = item - p.item_off[lo];
   const int split = local / p.Hkv;
   it.kvh = local - split * p.Hkv;
-  it.j0 = split * kDecSplit;
-  it.j1 = min(nk, it.j0 + kDecSplit);
-  (void)ns;
+  it.j0 = split * p.split;
+  it.j1 = min(nk, it.j0 + p.split);
 }
 
 __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, uint64_t *bar,
@@ -115,7 +113,7 @@ __global__ void __launch_bounds__(1024) dec_prologue_kernel(const __grid_constan
       item_off[s] = (int32_t)min(items, (long long)INT_MAX);
       bm_off[s] = words;
       tiles += nk;
-      if (Lq > 0) items += (long long)p.Hkv * ((nk + kDecSplit - 1) / kDecSplit);
+      if (Lq > 0) items += (long long)p.Hkv * ((nk + p.split - 1) / p.split);
       words += (long long)p.Hq * nq * ((nk + 31) / 32);
     }
     tile_off[p.n_seqs] = tiles;
@@ -381,6 +379,7 @@ dec_pv_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUten
       lready[2], lfree[2], drain;
   __shared__ int klist[2][kDecSplit];
   __shared__ uint32_t kact[2][kDecSplit];
+  __shared__ uint32_t act_sh[kDecSplit];
   __shared__ int nkept_sh[2];
   __shared__ uint32_t tmem_sh;
   __shared__ volatile int abort_sh;
@@ -540,21 +539,24 @@ dec_pv_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUten
         predmask[t] = bits;
       }
       named_bar_sync(1, kEpi);
+      if (t < nt) {   // heads of the group that keep tile j0 + t
+        uint32_t act = 0;
+        for (int g = 0; g < p.group; ++g) {
+          bool keep = false;
+          for (int qi = 0; qi < it.Lq; ++qi) keep |= !((predmask[g * it.Lq + qi] >> t) & 1u);
+          if (keep) act |= 1u << g;
+        }
+        act_sh[t] = act;
+      }
+      named_bar_sync(1, kEpi);
       if (t == 0) {
         int n = 0;
-        for (int u = 0; u < nt; ++u) {
-          uint32_t act = 0;   // heads of the group that keep tile j0 + u
-          for (int g = 0; g < p.group; ++g) {
-            bool keep = false;
-            for (int qi = 0; qi < it.Lq; ++qi) keep |= !((predmask[g * it.Lq + qi] >> u) & 1u);
-            if (keep) act |= 1u << g;
-          }
-          if (act) {
+        for (int u = 0; u < nt; ++u)
+          if (act_sh[u]) {
             klist[par][n] = it.j0 + u;
-            kact[par][n] = act;
+            kact[par][n] = act_sh[u];
             ++n;
           }
-        }
         nkept_sh[par] = n;
         mbar_arrive(&lready[par]);
       }
@@ -688,7 +690,7 @@ __global__ void __launch_bounds__(4 * kTile) dec_combine_kernel(const __grid_con
   if (qi >= Lq) return;
   const int t = threadIdx.x, c = t & (kTile - 1), grp = t >> 7, lane = t & 31, warp = t >> 5;
   const int Lk = p.cu_k[s + 1] - p.cu_k[s];
-  const int nk = (Lk + kTile - 1) / kTile, ns = (nk + kDecSplit - 1) / kDecSplit;
+  const int nk = (Lk + kTile - 1) / kTile, ns = (nk + p.split - 1) / p.split;
   const int kvh = h / p.group, r = (h - kvh * p.group) * Lq + qi;
   const int64_t it0 = (int64_t)p.item_off[s] + kvh;   // split q is item it0 + q * Hkv
   const int64_t H = p.Hkv;
@@ -741,7 +743,7 @@ size_t pv_smem_bytes(int RB) {
 cudaError_t launch_decode(const DecParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                           int sm_count, cudaStream_t stream) {
   const int64_t max_tiles = p.total_k / kTile + p.n_seqs;
-  const int64_t max_items = (int64_t)p.Hkv * (max_tiles / kDecSplit + p.n_seqs);
+  const int64_t max_items = (int64_t)p.Hkv * (max_tiles / p.split + p.n_seqs);
   const int grid = (int)(max_items < 8LL * sm_count ? max_items : 8LL * sm_count);
   dec_prologue_kernel<<<1, 1024, 0, stream>>>(p);
   if (p.rows <= 16)

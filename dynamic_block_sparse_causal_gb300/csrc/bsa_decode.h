@@ -10,20 +10,22 @@
 
 namespace bsa {
 
-constexpr int kDecSplit = 16;      // key tiles per work item of the split passes
+constexpr int kDecSplit = 16;      // most key tiles per work item of the split passes
 constexpr int kDecMaxRows = 32;    // query rows per (sequence, KV head): group x Lq
 constexpr int kDecThreads = 256;       // P V pass
 constexpr int kDecScoreThreads = 128;  // score pass: one thread per key of a tile
 
 // Per-stream scratch of the decode path. Tables follow the header:
 //   int64 tile_off[n_seqs + 1]   first key tile of every sequence (packed)
-//   int32 item_off[n_seqs + 1]   first work item (KV head x split) of every sequence
+//   int32 item_off[n_seqs + 1]   first work item (KV head x split) of every sequence;
+//                                a split is 8 or 16 key tiles (the host picks 8 when
+//                                16-tile splits would leave SMs idle)
 //   int64 bm_off[n_seqs + 1]     first skip-bitmap word of every sequence
 //   float S[tiles][Hkv][rows][128]  scaled scores (log2 units), -inf where masked
 //   float rm[Hkv][tiles][rows]      their row maxima per tile
 //   float pO[items][rows][128], pm[items][rows], pl[items][rows]
 //                                   per-split output, reference max, sum
-// with tiles <= total_k / 128 + n_seqs and items <= Hkv (tiles / 16 + n_seqs).
+// with tiles <= total_k / 128 + n_seqs and items <= Hkv (tiles / split + n_seqs).
 struct alignas(128) DecWorkspace {
   int32_t total_items;   // 0 when the arguments were rejected on the device
   int32_t pad_[31];
@@ -32,10 +34,10 @@ struct alignas(128) DecWorkspace {
 struct DecLayout {
   size_t tile_off, item_off, bm_off, S, rm, pO, pm, pl, bytes;
   int64_t max_tiles, max_items;
-  static DecLayout make(int n_seqs, int Hq, int Hkv, int rows, int64_t total_k) {
+  static DecLayout make(int n_seqs, int Hq, int Hkv, int rows, int64_t total_k, int split) {
     DecLayout l;
     l.max_tiles = total_k / kTile + n_seqs;
-    l.max_items = (int64_t)Hkv * (l.max_tiles / kDecSplit + n_seqs);
+    l.max_items = (int64_t)Hkv * (l.max_tiles / split + n_seqs);
     auto up = [](size_t x) { return (x + 127) / 128 * 128; };
     size_t off = sizeof(DecWorkspace);
     l.tile_off = off;
@@ -73,6 +75,7 @@ struct DecParams {
   int64_t total_k;
   int64_t max_tiles;          // rows of the rm table per KV head
   int32_t n_seqs, Hq, Hkv, group, rows, max_q, causal;
+  int32_t split;              // key tiles per split: 8 or 16
   float c, log2_lambda;
   uint64_t wait_limit_ns;
 };

@@ -101,6 +101,18 @@ def test_decode_batch_of_four_32k():
     print(_gpu.compare(p, g))
 
 
+def test_decode_sixteen_tile_splits():
+    """Enough keys that the library splits them 16 tiles at a time (smaller
+    batches get 8-tile splits): 16 KV heads x 80K keys."""
+    base = gi.packed("dec16", [40000, 40064], Hq=32, Hkv=16, seed=4, window=2.0,
+                     window_period=4096, window_len=512)
+    p = gi.chunk(base, [1, 2])
+    for lam in (0.005, 0.0):
+        g, st = run_decode(p, lam)
+        assert st == 0
+        print(lam, _gpu.compare(p, g))
+
+
 def test_decode_rejects_bad_lengths():
     b = _gpu.bsa()
     p = gi.chunk(_cases.small_problem("gqa4"), [4, 1])
