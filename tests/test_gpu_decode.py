@@ -113,6 +113,17 @@ def test_decode_sixteen_tile_splits():
         print(lam, _gpu.compare(p, g))
 
 
+def test_decode_batch_with_query_free_sequences():
+    """Sequences without new queries in the batch (Lq = 0) take no work and no
+    bitmap words; the others are unaffected."""
+    base = _cases.small_problem("gqa_ragged")             # lengths 300, 1000, 129, 640
+    p = gi.chunk(base, [1, 0, 2, 0])
+    for lam in (0.005, 0.0):
+        g, st = run_decode(p, lam)
+        assert st == 0
+        _gpu.compare(p, g)
+
+
 def test_decode_rejects_bad_lengths():
     b = _gpu.bsa()
     p = gi.chunk(_cases.small_problem("gqa4"), [4, 1])

@@ -193,6 +193,13 @@ def test_selection_packed_batch_and_edges():
     check_selection(x, cu, 0.8, order, nsel, None)
 
 
+def test_selection_tiny_p_keeps_the_top_block():
+    x = np.array([0.125, 0.5, 0.25, 0.125], np.float32)
+    order, nsel, keep, st = run_top_p(x, np.array([0, 500], np.int32), 1e-6)
+    assert st == 0 and nsel[0] == 1 and order.tolist() == [1, 2, 0, 3]
+    assert keep.tolist() == [0, 1, 0, 0]
+
+
 def test_selection_p_one_drops_trailing_zeros():
     x = np.array([0.0, 0.25, 0.0, 0.5, 0.0], np.float32)
     order, nsel, keep, st = run_top_p(x, np.array([0, 600], np.int32), 1.0)
