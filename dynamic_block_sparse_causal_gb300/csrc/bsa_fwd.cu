@@ -12,7 +12,7 @@
 //  * prologue_kernel (1 CTA): validates cu_seqlens, orders sequences longest
 //    first, builds the work-item level table and the skip-bitmap offsets,
 //    and writes the TMA tensor maps with the token extent patched in.
-//  * fwd_kernel<FP8> (persistent, one CTA per SM, 384 threads):
+//  * fwd_kernel<FP8, SKIP> (persistent, one CTA per SM, 384 threads):
 //      warp 0  lane 0   TMA producer: Q tiles, the K ring (3 stages), and,
 //                       when skipping is off, V with every K
 //      warp 1  lane 0   tcgen05 MMA issuer; with skipping on it also requests
@@ -342,14 +342,18 @@ __device__ __forceinline__ void mask_chunk(uint32_t (&v)[32], int ch, bool diag,
 
 }  // namespace
 
-template <bool FP8>
+// SKIP: the skip rule is on (lambda > 0). Each mode is its own instantiation,
+// so the code generated for one carries no branch of the other.
+template <bool FP8, bool SKIP>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = Cfg<FP8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar[B_COUNT];
   __shared__ uint32_t tmem_sh;
   __shared__ int item_sh[2][10];
-  __shared__ volatile int vote_sh[2];
+  // keep_sh[s][j & 1] != 0: some row of slot s keeps key tile j (one bit per warp
+  // that keeps it); the MMA warp reads it after the slot's four vote arrivals
+  __shared__ volatile uint32_t keep_sh[2][2];
   __shared__ volatile int abort_sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -359,10 +363,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   Workspace *ws = p.ws;
   const int total_items = ws->total_items, maxn = ws->max_tiles, T = ws->total_tokens;
   const uint64_t limit = p.wait_limit_ns;
-  const bool v_prefetch = !(p.log2_lambda > -INFINITY);   // no skipping: V streams with K
+  constexpr bool v_prefetch = !SKIP;   // no skipping: V streams with K
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < B_COUNT; ++b) mbar_init(&bar[b], 1);
+    for (int b = 0; b < B_COUNT; ++b)
+      mbar_init(&bar[b], (b == B_VOTE || b == B_VOTE + 1) ? 4 : 1);   // a vote: one arrival per warp
+    keep_sh[0][0] = keep_sh[0][1] = keep_sh[1][0] = keep_sh[1][1] = 0u;
     fence_mbar_init();
     abort_sh = 0;
   }
@@ -460,6 +466,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           return true;
         };
         do {
+          // no vote of this item is in flight yet (the item started after a CTA barrier)
+          keep_sh[0][0] = keep_sh[0][1] = keep_sh[1][0] = keep_sh[1][1] = 0u;
           // key tile 0 is never skipped: request its V before anything else
           if (!v_prefetch && !(ok = issue_v(0))) break;
           ok = mbar_wait(&bar[B_Q], qc & 1, limit, kSpinIssuer);
@@ -491,10 +499,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
               return true;
             };
             // ---- slot 0: vote, then P.V (if kept) before the next S overwrites P
-            ok = mbar_wait(&bar[B_VOTE + 0], vt0 & 1, limit, kSpinIssuer);
-            ++vt0;
-            if (!ok) break;
-            const bool keep0 = vote_sh[0] == 0;
+            bool keep0 = true;   // with skipping off every tile is kept
+            if (!v_prefetch) {
+              ok = mbar_wait(&bar[B_VOTE + 0], vt0 & 1, limit, kSpinIssuer);
+              ++vt0;
+              if (!ok) break;
+              keep0 = keep_sh[0][j & 1] != 0;
+              keep_sh[0][(j + 1) & 1] = 0u;   // tile j - 1's entry: read, and reused by j + 1
+            }
             if (keep0) {
               if (!vload && !(ok = issue_v(j))) break;
               vload = true;
@@ -517,10 +529,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             }
             // ---- slot 1
             if (has1) {
-              ok = mbar_wait(&bar[B_VOTE + 1], vt1 & 1, limit, kSpinIssuer);
-              ++vt1;
-              if (!ok) break;
-              const bool keep1 = vote_sh[1] == 0;
+              bool keep1 = true;
+              if (!v_prefetch) {
+                ok = mbar_wait(&bar[B_VOTE + 1], vt1 & 1, limit, kSpinIssuer);
+                ++vt1;
+                if (!ok) break;
+                keep1 = keep_sh[1][j & 1] != 0;
+                keep_sh[1][(j + 1) & 1] = 0u;
+              }
               if (keep1) {
                 if (!vload && !(ok = issue_v(j))) break;
                 vload = true;
@@ -623,14 +639,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           const float trm = rm * c;
           const bool pred = !valid || (trm < m2 + p.log2_lambda);
           tc_fence_before();
+          // each warp posts its vote as soon as it has it (the MMA warp acts on
+          // all four arrivals); the warpgroup's own decision is the barrier's
+          if (!v_prefetch) {   // with skipping off there is nothing to vote on
+            const bool wkeep = !__all_sync(0xffffffffu, pred);
+            if (lane == 0) {
+              if (wkeep) atomicOr(const_cast<uint32_t *>(&keep_sh[slot][j & 1]), 1u);
+              mbar_arrive(&bar[B_VOTE + slot]);
+            }
+          }
           const bool skip = bar_red_and(pred, barid, 128);
           if (abort_sh) {   // read after the barrier: uniform over the warpgroup
             ok = false;
             break;
-          }
-          if (row == 0) {
-            vote_sh[slot] = skip ? 1 : 0;
-            mbar_arrive(&bar[B_VOTE + slot]);
           }
           if (skip) {
             if (row == 0) word |= 1u << (j & 31);
@@ -793,20 +814,29 @@ size_t forward_smem_bytes() { return SM_BYTES + 1024; }
 
 cudaError_t launch_forward(const FwdParams &p, bool fp8, int num_ctas, cudaStream_t stream) {
   const size_t smem = forward_smem_bytes();
+  const bool skip = p.log2_lambda > -INFINITY;
   if (fp8) {
-    fwd_kernel<true><<<num_ctas, kFwdThreads, smem, stream>>>(p);
+    if (skip)
+      fwd_kernel<true, true><<<num_ctas, kFwdThreads, smem, stream>>>(p);
+    else
+      fwd_kernel<true, false><<<num_ctas, kFwdThreads, smem, stream>>>(p);
   } else {
-    fwd_kernel<false><<<num_ctas, kFwdThreads, smem, stream>>>(p);
+    if (skip)
+      fwd_kernel<false, true><<<num_ctas, kFwdThreads, smem, stream>>>(p);
+    else
+      fwd_kernel<false, false><<<num_ctas, kFwdThreads, smem, stream>>>(p);
   }
   return cudaGetLastError();
 }
 
 cudaError_t prepare_forward() {
   const int smem = (int)forward_smem_bytes();
-  cudaError_t e =
-      cudaFuncSetAttribute(fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<false, true>, a, smem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<false, false>, a, smem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<true, true>, a, smem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<true, false>, a, smem);
+  return e;
 }
 
 }  // namespace bsa
