@@ -595,6 +595,90 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           const int doff = off + (qi - j) * kTile;   // row r sees columns <= r + doff
           const bool diag = p.causal && doff < kTile - 1;
           const bool tailt = tail && j == nk - 1;
+          if (v_prefetch && have_kept) {
+            // ---- skipping off, after the first tile: one pass over S. P is
+            // computed against the current reference max while the row max is
+            // taken; only when a row's max outgrows the reference by more than
+            // 2^8 is O rescaled and the tile's P recomputed (S is still intact:
+            // P is stored at the end).
+            if (!mbar_wait(&bar[B_PV + slot], pvc & 1, limit)) abort_sh = 1;
+            ++pvc;
+            tc_fence_after();
+            constexpr int kPk = FP8 ? 8 : 16;   // packed words per 32-key chunk
+            uint32_t pk[4][kPk];
+            float psum[8];
+            auto exp_pass = [&](float nm, bool track, float &tm) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) psum[k] = 0.f;
+              float tmx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+              for (int ch = 0; ch < 4; ++ch) {
+                uint32_t v[32];
+                tmem_ld32(tS + ch * 32, v);
+                tmem_wait_ld(v);
+                if (diag || tailt) mask_chunk(v, ch, diag, tailt, row, doff, j * kTile, Lk);
+                float pv[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                  const float x = __uint_as_float(v[e]);
+                  if (track) tmx[e & 3] = fmaxf(tmx[e & 3], x);
+                  pv[e] = ex2_approx(fmaf(x, c, nm));
+                  psum[e & 7] += pv[e];
+                }
+#pragma unroll
+                for (int k = 0; k < kPk; ++k) {
+                  if (FP8)
+                    pk[ch][k] = (uint32_t)pack_e4m3x2(pv[4 * k], pv[4 * k + 1]) |
+                                ((uint32_t)pack_e4m3x2(pv[4 * k + 2], pv[4 * k + 3]) << 16);
+                  else
+                    pk[ch][k] = pack_bf16x2(pv[2 * k], pv[2 * k + 1]);
+                }
+              }
+              if (track) tm = fmaxf(fmaxf(tmx[0], tmx[1]), fmaxf(tmx[2], tmx[3]));
+            };
+            float rmax = -INFINITY;
+            exp_pass(valid ? -mref : -INFINITY, true, rmax);
+            const float mnew = valid ? fmaxf(m2, rmax * c) : 0.f;
+            const bool need = valid && (mnew - mref > kRescaleLog2);
+            if (__any_sync(0xffffffffu, need)) {
+              const float alpha = need ? ex2_approx(mref - mnew) : 1.f;
+              l *= alpha;
+              if (need) mref = mnew;
+#pragma unroll
+              for (int ch = 0; ch < 4; ++ch) {
+                uint32_t v[32];
+                tmem_ld32(tO + ch * 32, v);
+                tmem_wait_ld(v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                tmem_st32(tO + ch * 32, v);
+              }
+              float unused;
+              exp_pass(valid ? -mref : -INFINITY, false, unused);
+            }
+            m2 = mnew;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+              if (FP8)
+                tmem_st8(tS + ch * 8, reinterpret_cast<const uint32_t(&)[8]>(pk[ch]));
+              else
+                tmem_st16(tS + ch * 16, reinterpret_cast<const uint32_t(&)[16]>(pk[ch]));
+            }
+            tmem_wait_st();
+            l += ((psum[0] + psum[1]) + (psum[2] + psum[3])) + ((psum[4] + psum[5]) + (psum[6] + psum[7]));
+            tc_fence_before();
+            named_bar_sync(barid, 128);
+            if (abort_sh) {   // read after the barrier: uniform over the warpgroup
+              ok = false;
+              break;
+            }
+            if (row == 0) mbar_arrive(&bar[B_PRDY + slot]);
+            if (row == 0 && p.bitmap && (((j & 31) == 31) || j == last)) {
+              p.bitmap[boff + (j >> 5)] = word;
+              word = 0;
+            }
+            continue;
+          }
           float rm;
           {
             float acc[8];
