@@ -270,6 +270,15 @@ __device__ void fetch_item(const FwdParams &p, int total_items, int maxn, int *d
   dst[9] = p.cu_seqlens_k[s + 1] - ak;
 }
 
+// 32 lanes x 64 consecutive 32-bit columns in one load (two 32-register halves).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&a)[32], uint32_t (&b)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]),
+        "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]), "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]), "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31])
+      : "r"(taddr));
+}
+
 // Running row max over two 32-register chunks (three-input max, eight
 // independent chains).
 __device__ __forceinline__ void row_max64(float (&a)[8], const uint32_t (&v0)[32],
@@ -608,14 +617,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             uint32_t pk[4][kPk];
             float psum[8];
             auto exp_pass = [&](float nm, bool track, float &tm) {
+              uint32_t vnext[32];
 #pragma unroll
               for (int k = 0; k < 8; ++k) psum[k] = 0.f;
               float tmx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
               for (int ch = 0; ch < 4; ++ch) {
                 uint32_t v[32];
-                tmem_ld32(tS + ch * 32, v);
-                tmem_wait_ld(v);
+                if ((ch & 1) == 0) {   // chunks 2h, 2h + 1 in one 64-column load
+                  tmem_ld64(tS + ch * 32, v, vnext);
+                  tmem_wait_ld(v);
+                  reg_fence(vnext);
+                } else {
+#pragma unroll
+                  for (int e = 0; e < 32; ++e) v[e] = vnext[e];
+                }
                 if (diag || tailt) mask_chunk(v, ch, diag, tailt, row, doff, j * kTile, Lk);
                 float pv[32];
 #pragma unroll
@@ -706,8 +722,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               uint32_t v0[32], v1[32];
-              tmem_ld32(tS + half * 64, v0);
-              tmem_ld32(tS + half * 64 + 32, v1);
+              tmem_ld64(tS + half * 64, v0, v1);
               tmem_wait_ld(v0);
               reg_fence(v1);
               if (diag || tailt) {
