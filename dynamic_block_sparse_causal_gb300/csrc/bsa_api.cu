@@ -313,6 +313,7 @@ bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
   p.bm_off = reinterpret_cast<const int64_t *>(base + layout.bm_off);
   p.S = reinterpret_cast<float *>(base + layout.S);
   p.rm = reinterpret_cast<float *>(base + layout.rm);
+  p.smax = reinterpret_cast<float *>(base + layout.smax);
   p.pO = reinterpret_cast<float *>(base + layout.pO);
   p.pm = reinterpret_cast<float *>(base + layout.pm);
   p.pl = reinterpret_cast<float *>(base + layout.pl);
@@ -321,6 +322,7 @@ bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
   p.bitmap = skip_bitmap;
   p.total_k = total_k;
   p.max_tiles = layout.max_tiles;
+  p.max_splits = layout.max_items / Hkv;
   p.n_seqs = n_seqs;
   p.Hq = Hq;
   p.Hkv = Hkv;

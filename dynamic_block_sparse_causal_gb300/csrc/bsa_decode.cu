@@ -294,6 +294,7 @@ dec_scores_kernel(const __grid_constant__ DecParams p, const __grid_constant__ C
       named_bar_sync(1, kEpi);
       if (t == 0) mbar_arrive(&qready[par]);
       const int64_t toff = p.tile_off[it.s];
+      float split_max = -INFINITY;   // thread t < R: row t's max over this split
       for (int j = it.j0; j < it.j1; ++j, ++sc) {
         const uint32_t buf = sc & 1;
         ok = mbar_wait(&sfull[buf], (sc >> 1) & 1, limit);
@@ -332,9 +333,14 @@ dec_scores_kernel(const __grid_constant__ DecParams p, const __grid_constant__ C
           const float m = fmaxf(fmaxf(red[u & 1][0][t], red[u & 1][1][t]),
                                 fmaxf(red[u & 1][2][t], red[u & 1][3][t]));
           p.rm[(it.kvh * p.max_tiles + toff + j) * p.rows + t] = m;
+          split_max = fmaxf(split_max, m);
         }
       }
       if (stop) break;
+      // the split's row maxima, for the prefix max of the later splits
+      if (t < R)
+        p.smax[((int64_t)it.kvh * p.max_splits + p.item_off[it.s] / p.Hkv + it.j0 / p.split) *
+                   p.rows + t] = split_max;
     }
   }
   tc_fence_before();
@@ -507,16 +513,19 @@ dec_pv_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUten
       const uint32_t par = i & 1;
       const float *rmh = p.rm + ((int64_t)it.kvh * p.max_tiles + toff) * p.rows;
       // ---- decisions. Running max before the split: the max of the earlier
-      // tiles' row maxima. Rp (R rounded up to a power of two) divides the
-      // thread stride, so thread t always meets row t % Rp; the split's own
-      // maxima go to shared memory for the walk in order.
+      // splits' row maxima (written by the score pass). Rp (R rounded up to a
+      // power of two) divides the thread stride, so thread t always meets row
+      // t % Rp; the split's own tile maxima go to shared memory for the walk
+      // in order.
       const int Rp = R <= 1 ? 1 : 1 << (32 - __clz(R - 1));
       const int rt = t & (Rp - 1);
       float mp = -INFINITY;
       if (rt < R) {
-#pragma unroll 8
-        for (int idx = t; idx < it.j0 * Rp; idx += kEpi)
-          mp = fmaxf(mp, rmh[(int64_t)(idx / Rp) * p.rows + rt]);
+        const float *sm = p.smax + ((int64_t)it.kvh * p.max_splits + p.item_off[it.s] / p.Hkv) * p.rows;
+        const int q = it.j0 / p.split;   // splits before this one
+#pragma unroll 4
+        for (int idx = t; idx < q * Rp; idx += kEpi)
+          mp = fmaxf(mp, sm[(int64_t)(idx / Rp) * p.rows + rt]);
       }
       for (int idx = t; idx < nt * R; idx += kEpi)
         srm[idx] = rmh[(int64_t)(it.j0 + idx / R) * p.rows + idx % R];

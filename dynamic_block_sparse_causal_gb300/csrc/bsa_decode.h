@@ -23,6 +23,7 @@ constexpr int kDecScoreThreads = 128;  // score pass: one thread per key of a ti
 //   int64 bm_off[n_seqs + 1]     first skip-bitmap word of every sequence
 //   float S[tiles][Hkv][rows][128]  scaled scores (log2 units), -inf where masked
 //   float rm[Hkv][tiles][rows]      their row maxima per tile
+//   float smax[Hkv][splits][rows]   and per split (splits = items / Hkv)
 //   float pO[items][rows][128], pm[items][rows], pl[items][rows]
 //                                   per-split output, reference max, sum
 // with tiles <= total_k / 128 + n_seqs and items <= Hkv (tiles / split + n_seqs).
@@ -32,7 +33,7 @@ struct alignas(128) DecWorkspace {
 };
 
 struct DecLayout {
-  size_t tile_off, item_off, bm_off, S, rm, pO, pm, pl, bytes;
+  size_t tile_off, item_off, bm_off, S, rm, smax, pO, pm, pl, bytes;
   int64_t max_tiles, max_items;
   static DecLayout make(int n_seqs, int Hq, int Hkv, int rows, int64_t total_k, int split) {
     DecLayout l;
@@ -50,6 +51,8 @@ struct DecLayout {
     off += up((size_t)l.max_tiles * Hkv * rows * kTile * 4);
     l.rm = off;
     off += up((size_t)l.max_tiles * Hkv * rows * 4);
+    l.smax = off;
+    off += up((size_t)l.max_items * rows * 4);
     l.pO = off;
     off += up((size_t)l.max_items * rows * kTile * 4);
     l.pm = off;
@@ -68,12 +71,13 @@ struct DecParams {
   const int32_t *cu_q, *cu_k;
   const int64_t *tile_off, *bm_off;
   const int32_t *item_off;
-  float *S, *rm, *pO, *pm, *pl;
+  float *S, *rm, *smax, *pO, *pm, *pl;
   void *out;                  // bf16 [total_q, Hq, 128]
   float *lse;                 // [Hq, total_q] or null
   uint32_t *bitmap;           // or null
   int64_t total_k;
   int64_t max_tiles;          // rows of the rm table per KV head
+  int64_t max_splits;         // rows of the smax table per KV head
   int32_t n_seqs, Hq, Hkv, group, rows, max_q, causal;
   int32_t split;              // key tiles per split: 8 or 16
   float c, log2_lambda;

@@ -98,3 +98,57 @@ def test_paged_rejects_page_outside_pool():
     assert st == 0
     assert b.get_device_status() == 6
     assert bool((g_out == 5.0).all())
+
+
+def test_paged_fp8_equals_packed():
+    """FP8 E4M3 codes in the page pool (finite junk in unused slots): the paged
+    call equals the packed chunked FP8 call bit for bit and matches the oracle."""
+    import test_gpu_fp8
+    p = gi.chunk(_cases.small_problem("gqa_ragged"), [100, 777, 1, 200])
+    f8q, f8k, f8v = (test_gpu_fp8.gpu_quantize(x) for x in (p.q, p.k, p.v))
+    f8 = (f8q[0], f8k[0], f8v[0], f8q[1], f8k[1], f8v[1])
+    ref = _gpu.run(p, lam=0.05, fp8=f8)
+    rng = np.random.default_rng(3)
+    cuk = p.cu_seqlens_k
+    lens = np.diff(cuk.astype(np.int64))
+    nk = (lens + 127) // 128
+    num_pages = int(nk.sum()) + 3
+    max_pages = int(nk.max()) + 1
+    order = rng.permutation(num_pages)
+    junk = rng.integers(0, 0x7F, (num_pages, 128, p.Hkv, p.d)).astype(np.uint8)   # finite codes
+    junk |= (rng.integers(0, 2, junk.shape) << 7).astype(np.uint8)                  # either sign
+    kc, vc = junk.copy(), junk[::-1].copy()
+    table = np.full((p.n_seqs, max_pages), -1, np.int32)
+    nxt = 0
+    for s, L in enumerate(lens):
+        a = int(cuk[s])
+        for j in range(int(nk[s])):
+            pg = int(order[nxt])
+            nxt += 1
+            table[s, j] = pg
+            t0, t1 = j * 128, min(j * 128 + 128, int(L))
+            kc[pg, :t1 - t0] = f8k[0][a + t0:a + t1]
+            vc[pg, :t1 - t0] = f8v[0][a + t0:a + t1]
+    b = _gpu.bsa()
+    scales = [torch.from_numpy(np.asarray(x[1], np.float32)).cuda() for x in (f8q, f8k, f8v)]
+    b.check(b.set_fp8_scales(*scales), "scales")
+    try:
+        T = p.total_tokens
+        out = torch.full((T, p.Hq, p.d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((p.Hq, T), float("nan"), dtype=torch.float32, device="cuda")
+        nw = b.skip_bitmap_words_chunked(p.cu_seqlens, cuk, p.Hq)
+        bm = torch.full((max(nw, 1),), -1, dtype=torch.int32, device="cuda")
+        st = b.prefill_fwd_paged(torch.from_numpy(f8q[0]).cuda(), torch.from_numpy(kc).cuda(),
+                                 torch.from_numpy(vc).cuda(), torch.from_numpy(table).cuda(),
+                                 max_pages, num_pages, torch.from_numpy(p.cu_seqlens).cuda(),
+                                 torch.from_numpy(cuk).cuda(), p.n_seqs, p.Hq, p.Hkv, p.d, 1, 0.05,
+                                 b.BSA_FP8_E4M3, out, lse, bm)
+        b.check(st, "paged fp8")
+        torch.cuda.synchronize()
+        b.check(b.get_device_status(), "device status")
+    finally:
+        b.check(b.set_fp8_scales(None, None, None), "clear scales")
+    assert torch.equal(out, ref["out"]) and torch.equal(lse, ref["lse"])
+    g = dict(out=out, lse=lse, bitmap=bm[:nw].cpu().numpy().view(np.uint32), lam=0.05, causal=True)
+    assert np.array_equal(g["bitmap"], ref["bitmap"])
+    _gpu.compare(p, g, fp8=f8)
