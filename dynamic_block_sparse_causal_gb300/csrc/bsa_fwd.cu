@@ -175,6 +175,9 @@ constexpr uint32_t SM_Q0 = 0, SM_Q1 = kRegion, SM_K = 2 * kRegion,
 constexpr float kRescaleLog2 = 8.0f;  // lazy O rescale once m grows by 2^8
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kColS = 0, kColO = 256;   // TMEM: S_s at s*128, O_s at 256 + s*128
+// warp roles: TMA producer, MMA issuer, item fetch, then (from warp 4) the
+// softmax warpgroups of query slots 0 and 1 (warp w reaches TMEM lanes 32 (w % 4) ..)
+constexpr int kWarpProd = 0, kWarpMma = 1, kWarpFetch = 2, kWarpSoftmax = 4;
 
 // barrier slots
 enum : int {
@@ -364,6 +367,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   // that keeps it); the MMA warp reads it after the slot's four vote arrivals
   __shared__ volatile uint32_t keep_sh[2][2];
   __shared__ volatile int abort_sh;
+  // last load issued into each K stage, V stage and the Q slot (-1: none), for
+  // the bounded drain after a time-out
+  __shared__ int kc_last[kKStages], vc_last[kVStages], qc_last;
+  // Pipeline counters, persistent across items: each role keeps its own here
+  // between items and in registers within one, so that no role carries another
+  // role's counters in its registers.
+  //   [0, 3)    producer: Q, K, V loads
+  //   [3, 9)    MMA warp: Q, K, V, votes of slots 0 / 1, P-ready of slots 0 / 1
+  //   [12 + 4 s, 14 + 4 s)  softmax slot s: S tiles, P.V waits
+  __shared__ uint32_t ctr_sh[20];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t raw = smem_u32(smem_raw);
@@ -380,13 +393,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     keep_sh[0][0] = keep_sh[0][1] = keep_sh[1][0] = keep_sh[1][1] = 0u;
     fence_mbar_init();
     abort_sh = 0;
+    for (int k = 0; k < 20; ++k) ctr_sh[k] = 0u;
+    for (int st = 0; st < kKStages; ++st) kc_last[st] = -1;
+    for (int st = 0; st < kVStages; ++st) vc_last[st] = -1;
+    qc_last = -1;
   }
-  if (threadIdx.x == 64) fetch_item(p, total_items, maxn, item_sh[0]);
-  if (warp == 1) {
+  if (threadIdx.x == kWarpFetch * 32) fetch_item(p, total_items, maxn, item_sh[0]);
+  if (warp == kWarpMma) {
     tmem_alloc(&tmem_sh, 512);
     tmem_relinquish();
   }
-  if ((warp == 0 || warp == 1) && lane == 0) {
+  if ((warp == kWarpProd || warp == kWarpMma) && lane == 0) {
     tensormap_acquire(&ws->tmap[0]);
     tensormap_acquire(&ws->tmap[1]);
     tensormap_acquire(&ws->tmap[2]);
@@ -396,11 +413,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = tmem_sh;
 
-  // pipeline counters, persistent across items (each role keeps its own)
-  uint32_t kc = 0, vc = 0, qc = 0, vt0 = 0, vt1 = 0, pr0 = 0, pr1 = 0, sc = 0, pvc = 0;
-  int kc_last[kKStages] = {-1, -1, -1};
-  int vc_last[kVStages] = {-1, -1};
-  int qc_last = -1;
 
   for (int it = 0;; ++it) {
     const int *I = item_sh[it & 1];
@@ -419,9 +431,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     };
     bool ok = true;
 
-    if (warp == 0) {
+    if (warp == kWarpProd) {
       if (lane == 0) {
         // ------------------------------------------------ TMA producer
+        uint32_t qc = ctr_sh[0], kc = ctr_sh[1], vc = ctr_sh[2];
         const void *tq = &ws->tmap[0], *tk = &ws->tmap[1], *tv = &ws->tmap[2];
         mbar_expect_tx(&bar[B_Q], (has1 ? 2 : 1) * C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b) {
@@ -455,10 +468,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             ++vc;
           }
         }
+        ctr_sh[0] = qc;
+        ctr_sh[1] = kc;
+        ctr_sh[2] = vc;
       }
-    } else if (warp == 1) {
+    } else if (warp == kWarpMma) {
       if (lane == 0) {
         // ------------------------------------------------ MMA issuer
+        uint32_t qc = ctr_sh[3], kc = ctr_sh[4], vc = ctr_sh[5];
+        uint32_t vt0 = ctr_sh[6], vt1 = ctr_sh[7], pr0 = ctr_sh[8], pr1 = ctr_sh[9];
         const void *tv = &ws->tmap[2];
         const uint32_t S0 = tmem + kColS, S1 = tmem + kColS + 128;
         const uint32_t O0 = tmem + kColO, O1 = tmem + kColO + 128;
@@ -573,15 +591,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             }
           }
         } while (false);
+        ctr_sh[3] = qc;
+        ctr_sh[4] = kc;
+        ctr_sh[5] = vc;
+        ctr_sh[6] = vt0;
+        ctr_sh[7] = vt1;
+        ctr_sh[8] = pr0;
+        ctr_sh[9] = pr1;
       }
-    } else if (warp == 2) {
+    } else if (warp == kWarpFetch) {
       if (lane == 0) fetch_item(p, total_items, maxn, item_sh[(it + 1) & 1]);
-    } else if (warp >= 4) {
+    } else if (warp >= kWarpSoftmax) {
       // -------------------------------------------------- softmax warpgroups
-      const int slot = (warp - 4) >> 2;
+      const int slot = (warp - kWarpSoftmax) >> 2;
       const int h = slot ? h1 : h0;
       if (h >= 0) {
-        const int row = threadIdx.x - 128 * (slot + 1);   // 0..127 = TMEM lane
+        const int row = threadIdx.x & 127;   // = TMEM lane
+        uint32_t sc = ctr_sh[12 + 4 * slot], pvc = ctr_sh[13 + 4 * slot];
         const uint32_t barid = 1 + slot;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + kColS + slot * 128 + lane_off;
@@ -878,6 +904,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           if (row == 0 && p.bitmap)
             for (int w = (last >> 5) + 1; w < W; ++w) p.bitmap[boff + w] = 0u;
         }
+        if (row == 0) {   // uniform over the warpgroup; read by all at the next item's start
+          ctr_sh[12 + 4 * slot] = sc;
+          ctr_sh[13 + 4 * slot] = pvc;
+        }
       }
     }
     if (!ok) abort_sh = 1;
@@ -890,15 +920,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   // Normal exit: every item ended fully drained. After a time-out, wait
   // (bounded) for this CTA's own copies and MMAs before giving TMEM back.
   if (abort_sh) {
-    if ((warp == 0 || warp == 1) && lane == 0) {
+    if ((warp == kWarpProd || warp == kWarpMma) && lane == 0) {
       for (int st = 0; st < kKStages; ++st)
-        if (warp == 0 && kc_last[st] >= 0)
+        if (warp == kWarpProd && kc_last[st] >= 0)
           mbar_wait(&bar[B_KF + st], (kc_last[st] / kKStages) & 1, limit);
       for (int st = 0; st < kVStages; ++st)
         if (vc_last[st] >= 0) mbar_wait(&bar[B_VF + st], (vc_last[st] / kVStages) & 1, limit);
-      if (warp == 0 && qc_last >= 0) mbar_wait(&bar[B_Q], qc_last & 1, limit);
+      if (warp == kWarpProd && qc_last >= 0) mbar_wait(&bar[B_Q], qc_last & 1, limit);
     }
-    if (warp == 1 && lane == 0) {
+    if (warp == kWarpMma && lane == 0) {
       mma_commit(&bar[B_DRAIN]);
       mbar_wait(&bar[B_DRAIN], 0, limit);
     }
@@ -906,7 +936,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
 }
 
 size_t forward_smem_bytes() { return SM_BYTES + 1024; }
