@@ -383,7 +383,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t *sptr = smem_raw + (sbase - raw);
   Workspace *ws = p.ws;
-  const int total_items = ws->total_items, maxn = ws->max_tiles, T = ws->total_tokens;
   const uint64_t limit = p.wait_limit_ns;
   constexpr bool v_prefetch = !SKIP;   // no skipping: V streams with K
 
@@ -398,7 +397,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     for (int st = 0; st < kVStages; ++st) vc_last[st] = -1;
     qc_last = -1;
   }
-  if (threadIdx.x == kWarpFetch * 32) fetch_item(p, total_items, maxn, item_sh[0]);
+  if (threadIdx.x == kWarpFetch * 32) fetch_item(p, ws->total_items, ws->max_tiles, item_sh[0]);
   if (warp == kWarpMma) {
     tmem_alloc(&tmem_sh, 512);
     tmem_relinquish();
@@ -600,7 +599,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         ctr_sh[9] = pr1;
       }
     } else if (warp == kWarpFetch) {
-      if (lane == 0) fetch_item(p, total_items, maxn, item_sh[(it + 1) & 1]);
+      if (lane == 0) fetch_item(p, ws->total_items, ws->max_tiles, item_sh[(it + 1) & 1]);
     } else if (warp >= kWarpSoftmax) {
       // -------------------------------------------------- softmax warpgroups
       const int slot = (warp - kWarpSoftmax) >> 2;
@@ -612,13 +611,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + kColS + slot * 128 + lane_off;
         const uint32_t tO = tmem + kColO + slot * 128 + lane_off;
-        const int qpos = qi * kTile + row;
-        const bool valid = qpos < L;
+        const bool valid = qi * kTile + row < L;
         const bool tail = !p.causal && (Lk % kTile) != 0;
         float c = p.c;
         if (FP8) c *= p.q_scale[h] * p.k_scale[kvh];
         const int W = (nk + 31) >> 5;
-        const long long boff = p.seq_bitmap_off[s] + ((long long)h * nq + qi) * W;
+        // this row's skip-bitmap words
+        uint32_t *const brow =
+            p.bitmap ? p.bitmap + p.seq_bitmap_off[s] + ((long long)h * nq + qi) * W : nullptr;
+        const int doff0 = off + qi * kTile;   // row r of key tile j sees columns <= r + doff0 - 128 j
         float m2 = -INFINITY, mref = 0.f, l = 0.f;
         uint32_t word = 0;
         bool have_kept = false;
@@ -627,7 +628,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           if (!mbar_wait(&bar[B_SF + slot], sc & 1, limit, kSpinSoftmax)) abort_sh = 1;
           ++sc;
           tc_fence_after();
-          const int doff = off + (qi - j) * kTile;   // row r sees columns <= r + doff
+          const int doff = doff0 - j * kTile;   // row r sees columns <= r + doff
           const bool diag = p.causal && doff < kTile - 1;
           const bool tailt = tail && j == nk - 1;
           if (v_prefetch && have_kept) {
@@ -715,8 +716,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
               break;
             }
             if (row == 0) mbar_arrive(&bar[B_PRDY + slot]);
-            if (row == 0 && p.bitmap && (((j & 31) == 31) || j == last)) {
-              p.bitmap[boff + (j >> 5)] = word;
+            if (row == 0 && brow && (((j & 31) == 31) || j == last)) {
+              brow[j >> 5] = word;
               word = 0;
             }
             continue;
@@ -869,8 +870,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             if (row == 0) mbar_arrive(&bar[B_PRDY + slot]);
             have_kept = true;
           }
-          if (row == 0 && p.bitmap && (((j & 31) == 31) || j == last)) {
-            p.bitmap[boff + (j >> 5)] = word;
+          if (row == 0 && brow && (((j & 31) == 31) || j == last)) {
+            brow[j >> 5] = word;
             word = 0;
           }
         }
@@ -879,10 +880,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           if (!mbar_wait(&bar[B_PV + slot], pvc & 1, limit)) abort_sh = 1;
           ++pvc;
           tc_fence_after();
+          // the item's fields again from shared memory (not kept in registers
+          // through the tile loop)
+          const volatile int *Iv = item_sh[it & 1];
+          const int ea = Iv[6], eh = Iv[3 + slot], ekvh = Iv[2];
+          const int tok = ea + Iv[5] * kTile + row;   // this row's query token
           float inv = 0.f;
-          if (valid && l > 0.f) inv = (FP8 ? p.v_scale[kvh] : 1.f) / l;
+          if (valid && l > 0.f) inv = (FP8 ? p.v_scale[ekvh] : 1.f) / l;
           __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
-                                ((size_t)(a + qpos) * p.Hq + h) * kHeadDim;
+                                ((size_t)tok * p.Hq + eh) * kHeadDim;
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             uint32_t v[32];
@@ -900,9 +906,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
                 dst[q] = make_uint4(w2[4 * q], w2[4 * q + 1], w2[4 * q + 2], w2[4 * q + 3]);
             }
           }
-          if (valid && p.lse) p.lse[(size_t)h * T + a + qpos] = (mref + log2f(l)) * kLn2;
-          if (row == 0 && p.bitmap)
-            for (int w = (last >> 5) + 1; w < W; ++w) p.bitmap[boff + w] = 0u;
+          if (valid && p.lse) p.lse[(size_t)eh * ws->total_tokens + tok] = (mref + log2f(l)) * kLn2;
+          if (row == 0 && brow)
+            for (int w = (last >> 5) + 1; w < W; ++w) brow[w] = 0u;
         }
         if (row == 0) {   // uniform over the warpgroup; read by all at the next item's start
           ctr_sh[12 + 4 * slot] = sc;
