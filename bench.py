@@ -295,7 +295,7 @@ def gpu_arm(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     bsa.lib()
-    p = gi.config(args.config, seed=args.seed, lam=args.lam)
+    p = gi.config(args.config, seed=args.seed, lam=args.lam, sink=args.sink)
     seqlens = [int(x) for x in p.seqlens]
     T, Hq, Hkv, d = p.total_tokens, p.Hq, p.Hkv, p.d
     dflops = dense_flops(seqlens, Hq, d)
@@ -407,6 +407,19 @@ def gpu_arm(args, rank, world, local_rank):
         bsa.check(bsa.get_device_status(stream), "device status")
         del codes, scales
 
+    def time_fn(fn, n):
+        """Mean ms of n calls on the stream after 3 untimed ones (CUDA events)."""
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
     # next rows: chunked prefill (the last 8192 queries against all keys) and
     # the same chunk with K/V in a shuffled pool of 128-token pages
     rows = None
@@ -452,18 +465,6 @@ def gpu_arm(args, rank, world, local_rank):
                           "ms": round(m, 3), "dense_equiv_tflops": round(cf / m / 1e9, 1)}
         bsa.check(bsa.get_device_status(stream), "device status")
         del kpool, vpool
-
-        def time_fn(fn, n):
-            for _ in range(3):
-                fn()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(n):
-                fn()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            return e0.elapsed_time(e1) / n
 
         # decode (one new query per sequence, the deployment guide's decode
         # threshold 0.005) through bsa_decode_fwd, the split-KV path, on the
@@ -535,6 +536,33 @@ def gpu_arm(args, rank, world, local_rank):
             "mma_tflops": round(mma_flops / mi / 1e9, 1), "mma_frac": round(mma_flops / mi / 1e9 / peak, 4),
             "launches": 5}
 
+    # diagnostic, not the headline: the 32K layer with a weak sink (0.25 u),
+    # where about two thirds of the causal tiles are skipped and the kept-tile
+    # path (exponentials, V loads, P.V) carries a third of the work
+    diag = None
+    if not args.no_rows and args.config == "C2" and args.sink == 4.0:
+        pd = gi.config("C1", seed=args.seed, lam=args.lam, sink=0.25)
+        sl = [int(x) for x in pd.seqlens]
+        Td = pd.total_tokens
+        qd, kd, vd = upload(pd.q), upload(pd.k), upload(pd.v)
+        cud = torch.from_numpy(pd.cu_seqlens).to(dev)
+        outd = torch.empty((Td, Hq, d), dtype=torch.bfloat16, device=dev)
+        lsed = torch.empty((Hq, Td), dtype=torch.float32, device=dev)
+        bmd = torch.empty((bsa.skip_bitmap_words(pd.cu_seqlens, Hq),), dtype=torch.int32, device=dev)
+
+        def diag_step():
+            bsa.check(bsa.prefill_fwd(qd, kd, vd, cud, pd.n_seqs, Hq, Hkv, d, 1, args.lam, bsa.BSA_BF16,
+                                      outd, lsed, bmd, stream), "bsa_prefill_fwd (diagnostic)")
+        md = time_fn(diag_step, max(args.steps, 10))
+        bsa.check(bsa.get_device_status(stream), "device status")
+        skd = popcount(bmd.cpu().numpy())
+        xd = executed_flops(sl, Hq, skd, d)
+        diag = {"workload": "32K layer (Llama-3-8B heads), sink 0.25 u instead of 4 u", "lambda": args.lam,
+                "ms": round(md, 3), "skip_fraction": round(skd / causal_tiles(sl, Hq), 5),
+                "dense_equiv_tflops": round(dense_flops(sl, Hq, d) / md / 1e9, 1),
+                "executed_tflops": round(xd / md / 1e9, 1), "roofline_frac": round(xd / md / 1e9 / peak, 4)}
+        del qd, kd, vd, outd, lsed, bmd
+
     # dense causal attention from the box's library (torch SDPA) on the same
     # shape: the comparison for the lambda = 0 path
     dense_ref = None
@@ -565,44 +593,86 @@ def gpu_arm(args, rank, world, local_rank):
         except Exception as e:  # a missing backend is reported, not fatal
             dense_ref = {"impl": "torch SDPA", "error": str(e)[:200]}
 
-    # end to end through the C interface with host buffers
+    # end to end through the C interface with host buffers: every step copies
+    # its inputs in from pinned host memory and its results (out, lse, skip
+    # bitmap) back out. Two device buffer sets and two host result sets let
+    # step i + 1's upload and step i - 1's download run on copy streams while
+    # step i computes; the timed region includes the first upload and the
+    # last download. The same steps run back to back on one stream are
+    # reported beside it.
     e2e = None
     if not args.no_e2e:
         hq = torch.from_numpy(p.q.view(np.int16)).pin_memory()
         hk = torch.from_numpy(p.k.view(np.int16)).pin_memory()
         hv = torch.from_numpy(p.v.view(np.int16)).pin_memory()
         hcu = torch.from_numpy(p.cu_seqlens).pin_memory()
-        hout = torch.empty((T, Hq, d), dtype=torch.int16).pin_memory()
-        hlse = torch.empty((Hq, T), dtype=torch.float32).pin_memory()
-        hbm = torch.empty((nw,), dtype=torch.int32).pin_memory()
+        hres = [(torch.empty((T, Hq, d), dtype=torch.int16).pin_memory(),
+                 torch.empty((Hq, T), dtype=torch.float32).pin_memory(),
+                 torch.empty((nw,), dtype=torch.int32).pin_memory()) for _ in range(2)]
+        dbuf = [(q, k, v, cu, out, lse, bm),
+                (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(cu),
+                 torch.empty_like(out), torch.empty_like(lse), torch.empty_like(bm))]
+        s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev = {n: [torch.cuda.Event(), torch.cuda.Event()] for n in ("up", "comp", "down")}
+        used = [False, False]
 
-        def e2e_step():
-            q.view(torch.int16).copy_(hq, non_blocking=True)
-            k.view(torch.int16).copy_(hk, non_blocking=True)
-            v.view(torch.int16).copy_(hv, non_blocking=True)
-            cu.copy_(hcu, non_blocking=True)
-            step()
-            hout.copy_(out.view(torch.int16), non_blocking=True)
-            hlse.copy_(lse, non_blocking=True)
-            hbm.copy_(bm, non_blocking=True)
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        n_e2e = max(2, args.steps // 2)
-        barrier(world)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for _ in range(n_e2e):
-            e2e_step()
-        torch.cuda.synchronize()
-        barrier(world)
-        ms_e2e = max_over_ranks((time.perf_counter() - t0) * 1e3 / n_e2e, world, dev)
+        def e2e_step(i, overlap=True):
+            bi = i % 2 if overlap else 0
+            dq, dk, dv, dcu, dout, dlse, dbm = dbuf[bi]
+            ho, hl, hb = hres[bi]
+            s_in = s_up if overlap else stream
+            s_out = s_down if overlap else stream
+            with torch.cuda.stream(s_in):
+                if used[bi]:
+                    s_in.wait_event(ev["comp"][bi])       # the forward that last read this set
+                dq.view(torch.int16).copy_(hq, non_blocking=True)
+                dk.view(torch.int16).copy_(hk, non_blocking=True)
+                dv.view(torch.int16).copy_(hv, non_blocking=True)
+                dcu.copy_(hcu, non_blocking=True)
+                ev["up"][bi].record(s_in)
+            stream.wait_event(ev["up"][bi])
+            if used[bi]:
+                stream.wait_event(ev["down"][bi])         # the download that last read out / lse / bitmap
+            st = bsa.prefill_fwd(dq, dk, dv, dcu, p.n_seqs, Hq, Hkv, d, 1, args.lam, bsa.BSA_BF16,
+                                 dout, dlse, dbm, stream)
+            if st != 0:
+                raise bsa.BsaError(st, "bsa_prefill_fwd")
+            ev["comp"][bi].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev["comp"][bi])
+                ho.copy_(dout.view(torch.int16), non_blocking=True)
+                hl.copy_(dlse, non_blocking=True)
+                hb.copy_(dbm, non_blocking=True)
+                ev["down"][bi].record(s_out)
+            used[bi] = True
+
+        def run_e2e(n, overlap):
+            for i in range(2):
+                e2e_step(i, overlap)
+            torch.cuda.synchronize()
+            barrier(world)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for i in range(n):
+                e2e_step(i, overlap)
+            torch.cuda.synchronize()
+            barrier(world)
+            return max_over_ranks((time.perf_counter() - t0) * 1e3 / n, world, dev)
+
+        n_e2e = max(4, args.steps // 2)
+        ms_e2e = run_e2e(n_e2e, True)
+        ms_serial = run_e2e(max(2, args.steps // 2), False)
         h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + hcu.numel() * 4
-        d2h = hout.numel() * 2 + hlse.numel() * 4 + hbm.numel() * 4
+        d2h = hres[0][0].numel() * 2 + hres[0][1].numel() * 4 + hres[0][2].numel() * 4
         e2e = {"value": round(dflops * world / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                "ms_per_step": round(ms_e2e, 3), "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h)}
+               "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
+               "overlap": "upload of step i+1 and download of step i-1 on copy streams during the "
+                          "forward of step i (two buffer sets); first upload and last download timed",
+               "serial_ms_per_step": round(ms_serial, 3),
+               "serial_value": round(dflops * world / (ms_serial * 1e-3) / 1e12, 2)}
         bsa.check(bsa.get_device_status(stream), "device status")
+        del dbuf, hres
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -617,13 +687,14 @@ def gpu_arm(args, rank, world, local_rank):
         "data": "synthetic (seeded generator: sink + local-window bias, Llama-3-8B attention shape)",
         "config": {"workload": WORKLOADS.get(args.config, args.config), "name": args.config,
                    "tokens": T, "Hq": Hq, "Hkv": Hkv, "d": d, "lambda": args.lam, "causal": True,
+                   "sink": args.sink,
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (q/out 1.07 GB each, k/v 0.27 GB each); no flush"},
         "skip_fraction": round(skipped / ctiles, 5), "executed_tflop_per_step": round(xflops / 1e12, 3),
         "dense_equiv_tflop_per_step": round(dflops / 1e12, 3),
         "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
         "gpu_launches": 2 * args.steps, "lambda_sweep": sweep, "dense_reference": dense_ref,
-        "fp8": fp8, "next_rows": rows,
+        "fp8": fp8, "next_rows": rows, "diagnostic_weak_sink": diag,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -637,7 +708,7 @@ def reference_arm(args, rank, world):
     if rank != 0:
         return
     from gen import inputs as gi
-    p = gi.config(args.config, seed=args.seed, lam=args.lam)
+    p = gi.config(args.config, seed=args.seed, lam=args.lam, sink=args.sink)
     vals = []
     saved = SavedLayer(p)
     try:
@@ -677,6 +748,8 @@ def main(argv=None):
     ap.add_argument("--config", default="C2", choices=sorted(WORKLOADS))
     ap.add_argument("--lam", type=float, default=0.01)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--sink", type=float, default=4.0,
+                    help="sink strength of the input recipe (4.0; smaller keeps more tiles)")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
