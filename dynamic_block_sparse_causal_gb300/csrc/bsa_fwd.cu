@@ -168,10 +168,15 @@ namespace {
 
 constexpr uint32_t kRegion = 32768;   // one bf16 tile slot in shared memory
 constexpr uint32_t kBox = 16384;      // one 128-row x 128-byte TMA box
-constexpr int kKStages = 3;           // K ring depth
-constexpr int kVStages = 2;           // V ring depth
-constexpr uint32_t SM_Q0 = 0, SM_Q1 = kRegion, SM_K = 2 * kRegion,
-                   SM_V = SM_K + kKStages * kRegion, SM_BYTES = SM_V + kVStages * kRegion;
+// K and V rings share five 32 KiB regions after the two Q tiles: 3 K + 2 V
+// stages with skipping off (V streams with every K), 4 K + 1 V with it on
+// (V is loaded only for kept tiles, K for every tile)
+constexpr int kKStages = 4, kVStages = 2;   // the deeper of the two, for barrier slots
+template <bool SKIP>
+struct Ring {
+  static constexpr int K = SKIP ? 4 : 3, V = SKIP ? 1 : 2;
+};
+constexpr uint32_t SM_Q0 = 0, SM_Q1 = kRegion, SM_K = 2 * kRegion, SM_BYTES = SM_K + 5 * kRegion;
 constexpr float kRescaleLog2 = 8.0f;  // lazy O rescale once m grows by 2^8
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kColS = 0, kColO = 256;   // TMEM: S_s at s*128, O_s at 256 + s*128
@@ -359,6 +364,8 @@ __device__ __forceinline__ void mask_chunk(uint32_t (&v)[32], int ch, bool diag,
 template <bool FP8, bool SKIP>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = Cfg<FP8>;
+  constexpr int KST = Ring<SKIP>::K, VST = Ring<SKIP>::V;
+  constexpr uint32_t SM_V = SM_K + KST * kRegion;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar[B_COUNT];
   __shared__ uint32_t tmem_sh;
@@ -369,7 +376,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   __shared__ volatile int abort_sh;
   // last load issued into each K stage, V stage and the Q slot (-1: none), for
   // the bounded drain after a time-out
-  __shared__ int kc_last[kKStages], vc_last[kVStages], qc_last;
+  __shared__ int kc_last[kKStages], vc_last[kVStages], qc_last;   // sized for the deeper ring
   // Pipeline counters, persistent across items: each role keeps its own here
   // between items and in registers within one, so that no role carries another
   // role's counters in its registers.
@@ -393,8 +400,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     fence_mbar_init();
     abort_sh = 0;
     for (int k = 0; k < 20; ++k) ctr_sh[k] = 0u;
-    for (int st = 0; st < kKStages; ++st) kc_last[st] = -1;
-    for (int st = 0; st < kVStages; ++st) vc_last[st] = -1;
+    for (int st = 0; st < KST; ++st) kc_last[st] = -1;
+    for (int st = 0; st < VST; ++st) vc_last[st] = -1;
     qc_last = -1;
   }
   if (threadIdx.x == kWarpFetch * 32) fetch_item(p, ws->total_items, ws->max_tiles, item_sh[0]);
@@ -444,8 +451,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         }
         qc_last = (int)qc++;
         for (int j = 0; j <= last && ok; ++j) {
-          const uint32_t st = kc % kKStages;
-          ok = mbar_wait(&bar[B_KE + st], ((kc / kKStages) & 1) ^ 1, limit, kSpinIssuer);
+          const uint32_t st = kc % KST;
+          ok = mbar_wait(&bar[B_KE + st], ((kc / KST) & 1) ^ 1, limit, kSpinIssuer);
           if (!ok) break;
           if ((int)kc != p.debug_drop_k_load) {
             mbar_expect_tx(&bar[B_KF + st], C::kTileBytes);
@@ -456,8 +463,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           }
           ++kc;
           if (v_prefetch) {
-            const uint32_t vs = vc % kVStages;
-            ok = mbar_wait(&bar[B_VE + vs], ((vc / kVStages) & 1) ^ 1, limit, kSpinIssuer);
+            const uint32_t vs = vc % VST;
+            ok = mbar_wait(&bar[B_VE + vs], ((vc / VST) & 1) ^ 1, limit, kSpinIssuer);
             if (!ok) break;
             mbar_expect_tx(&bar[B_VF + vs], C::kTileBytes);
             for (int b = 0; b < C::kBoxes; ++b)
@@ -482,8 +489,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         const uint32_t q0s = sbase + SM_Q0, q1s = sbase + SM_Q1;
         // V_j request from this thread (skipping on): only kept tiles are loaded
         auto issue_v = [&](int j) -> bool {
-          const uint32_t vs = vc % kVStages;
-          if (!mbar_wait(&bar[B_VE + vs], ((vc / kVStages) & 1) ^ 1, limit, kSpinIssuer)) return false;
+          const uint32_t vs = vc % VST;
+          if (!mbar_wait(&bar[B_VE + vs], ((vc / VST) & 1) ^ 1, limit, kSpinIssuer)) return false;
           mbar_expect_tx(&bar[B_VF + vs], C::kTileBytes);
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_3d(sptr + SM_V + vs * kRegion + b * kBox, tv, &bar[B_VF + vs],
@@ -499,8 +506,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           ok = mbar_wait(&bar[B_Q], qc & 1, limit, kSpinIssuer);
           ++qc;
           if (!ok) break;
-          uint32_t st = kc % kKStages;
-          ok = mbar_wait(&bar[B_KF + st], (kc / kKStages) & 1, limit, kSpinIssuer);
+          uint32_t st = kc % KST;
+          ok = mbar_wait(&bar[B_KF + st], (kc / KST) & 1, limit, kSpinIssuer);
           if (!ok) break;
           tc_fence_after();
           uint32_t ks = sbase + SM_K + st * kRegion;
@@ -516,10 +523,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           for (int j = 0; j <= last && ok; ++j) {
             bool vload = v_prefetch || j == 0;   // V_j requested
             bool vready = false;                 // V_j landed (waited)
-            const uint32_t vs = vc % kVStages;
+            const uint32_t vs = vc % VST;
             auto wait_v = [&]() -> bool {
               if (vready) return true;
-              if (!mbar_wait(&bar[B_VF + vs], (vc / kVStages) & 1, limit, kSpinIssuer)) return false;
+              if (!mbar_wait(&bar[B_VF + vs], (vc / VST) & 1, limit, kSpinIssuer)) return false;
               tc_fence_after();
               vready = true;
               return true;
@@ -545,8 +552,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
               mma_commit(&bar[B_PV + 0]);
             }
             if (j < last) {
-              st = kc % kKStages;
-              ok = mbar_wait(&bar[B_KF + st], (kc / kKStages) & 1, limit, kSpinIssuer);
+              st = kc % KST;
+              ok = mbar_wait(&bar[B_KF + st], (kc / KST) & 1, limit, kSpinIssuer);
               if (!ok) break;
               tc_fence_after();
               ks = sbase + SM_K + st * kRegion;
@@ -927,11 +934,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   // (bounded) for this CTA's own copies and MMAs before giving TMEM back.
   if (abort_sh) {
     if ((warp == kWarpProd || warp == kWarpMma) && lane == 0) {
-      for (int st = 0; st < kKStages; ++st)
+      for (int st = 0; st < KST; ++st)
         if (warp == kWarpProd && kc_last[st] >= 0)
-          mbar_wait(&bar[B_KF + st], (kc_last[st] / kKStages) & 1, limit);
-      for (int st = 0; st < kVStages; ++st)
-        if (vc_last[st] >= 0) mbar_wait(&bar[B_VF + st], (vc_last[st] / kVStages) & 1, limit);
+          mbar_wait(&bar[B_KF + st], (kc_last[st] / KST) & 1, limit);
+      for (int st = 0; st < VST; ++st)
+        if (vc_last[st] >= 0) mbar_wait(&bar[B_VF + st], (vc_last[st] / VST) & 1, limit);
       if (warp == kWarpProd && qc_last >= 0) mbar_wait(&bar[B_Q], qc_last & 1, limit);
     }
     if (warp == kWarpMma && lane == 0) {
