@@ -753,7 +753,7 @@ cudaError_t launch_decode(const DecParams &p, const CUtensorMap &tk, const CUten
                           int sm_count, cudaStream_t stream) {
   const int64_t max_tiles = p.total_k / kTile + p.n_seqs;
   const int64_t max_items = (int64_t)p.Hkv * (max_tiles / p.split + p.n_seqs);
-  const int grid = (int)(max_items < 8LL * sm_count ? max_items : 8LL * sm_count);
+  const int grid = (int)(max_items < 4LL * sm_count ? max_items : 4LL * sm_count);
   dec_prologue_kernel<<<1, 1024, 0, stream>>>(p);
   if (p.rows <= 16)
     dec_scores_kernel<16><<<grid, kDecScoreThreads + 64, dec_smem_bytes(16), stream>>>(p, tk);
