@@ -13,10 +13,11 @@
 //    first, builds the work-item level table and the skip-bitmap offsets,
 //    and writes the TMA tensor maps with the token extent patched in.
 //  * fwd_kernel<FP8, SKIP> (persistent, one CTA per SM, 384 threads):
-//      warp 0  lane 0   TMA producer: Q tiles, the K ring (3 stages), and,
-//                       when skipping is off, V with every K
+//      warp 0  lane 0   TMA producer: Q tiles, the K ring (4 stages with
+//                       skipping on, 3 with it off), and, when skipping is off,
+//                       V with every K (2-stage ring)
 //      warp 1  lane 0   tcgen05 MMA issuer; with skipping on it also requests
-//                       V_j (2-stage ring) as soon as a query tile votes to keep j
+//                       V_j (one stage) as soon as a query tile votes to keep j
 //      warp 2  lane 0   fetches the next work item (atomic counter)
 //      warps 4-7        softmax warpgroup of query slot 0 (TMEM lanes 0-127)
 //      warps 8-11       softmax warpgroup of query slot 1
@@ -27,7 +28,13 @@
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512),
 // fp32, lane = query row; P_s (bf16 / e4m3) is written over the first
 // columns of S_s and read from there by the P.V MMA. Shared memory
-// (1024-aligned, 128-byte swizzle): Q0 Q1 K[3] V[2], 32 KiB each.
+// (1024-aligned, 128-byte swizzle), 32 KiB regions: Q0 Q1, then K[4] V[1]
+// with skipping on or K[3] V[2] with it off.
+//
+// Pipeline counters live in registers within a work item and in shared
+// memory between items, one set per role, so that no role's registers carry
+// another role's counters through the item loop (register pressure in the
+// softmax warpgroups sets the length of the per-tile chain).
 //
 // Per key tile j and query slot s the softmax warpgroup loads S_s from TMEM,
 // masks the diagonal / tail, takes the row max, and votes with one
