@@ -659,7 +659,7 @@ def gpu_arm(args, rank, world, local_rank):
             barrier(world)
             return max_over_ranks((time.perf_counter() - t0) * 1e3 / n, world, dev)
 
-        n_e2e = max(4, args.steps // 2)
+        n_e2e = max(4, args.steps)   # the first upload and last download amortise over these
         ms_e2e = run_e2e(n_e2e, True)
         ms_serial = run_e2e(max(2, args.steps // 2), False)
         h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + hcu.numel() * 4
