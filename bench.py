@@ -514,6 +514,7 @@ def gpu_arm(args, rank, world, local_rank):
 
         # UniPrefill block importance of the layer (last 64 queries, G = 128)
         # and the top-p (p = 0.9) selection over its head-mean scores
+        n_win = 64
         nb = bsa.importance_blocks(p.cu_seqlens)
         sc = torch.empty((Hq, nb), dtype=torch.float32, device=dev)
         mn = torch.empty((nb,), dtype=torch.float32, device=dev)
@@ -522,18 +523,22 @@ def gpu_arm(args, rank, world, local_rank):
         keep = torch.empty((nb,), dtype=torch.uint8, device=dev)
 
         def importance():
-            bsa.check(bsa.block_importance(q, k, cu, 1, Hq, Hkv, d, 64, 1, nb, sc, mn, stream), "importance")
+            bsa.check(bsa.block_importance(q, k, cu, 1, Hq, Hkv, d, n_win, 1, nb, sc, mn, stream), "importance")
 
         def select():
             bsa.check(bsa.top_p_select(mn, cu, 1, nb, 0.9, order, nsel, keep, stream), "top_p")
         mi = time_fn(importance, args.steps)
         ms_sel = time_fn(select, args.steps)
         bsa.check(bsa.get_device_status(stream), "device status")
-        mma_flops = Hq * nb * 2 * TILE * TILE * d          # 128-row tiles issued
+        # 128-row tiles issued: with a window of <= 64 rows and an even group
+        # one tile carries two query heads
+        pair = 2 if (n_win <= 64 and (Hq // Hkv) % 2 == 0) else 1
+        mma_flops = Hq // pair * nb * 2 * TILE * TILE * d
         rows["block_importance"] = {
             "workload": f"UniPrefill Eq. 3-4 on the layer: last 64 queries, {nb} blocks of 128 keys, {Hq} heads",
             "ms": round(mi, 4), "top_p_ms": round(ms_sel, 4), "p": 0.9, "kept_blocks": int(nsel[0]),
             "mma_tflops": round(mma_flops / mi / 1e9, 1), "mma_frac": round(mma_flops / mi / 1e9 / peak, 4),
+            "query_heads_per_tile": pair,
             "launches": 5}
 
     # diagnostic, not the headline: the 32K layer with a weak sink (0.25 u),

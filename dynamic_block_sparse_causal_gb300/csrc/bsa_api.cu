@@ -119,14 +119,15 @@ bsa_status_t imp_scratch_for(int dev, cudaStream_t stream, size_t bytes, void **
   return BSA_OK;
 }
 
-// [tokens, H, 128] tiles of 128 rows x 128 bytes, 128-byte swizzle. The token
+// [tokens, H, 128] tiles of 128 rows (or box_rows) x 128 bytes, 128-byte swizzle. The token
 // extent is a placeholder (1) that the prologue replaces with cu[n_seqs],
 // except for a paged K/V pool, whose extent (pages x 128) is known here.
-bool encode_tile_map(CUtensorMap *m, const void *base, int H, bool fp8, uint64_t tokens = 1) {
+bool encode_tile_map(CUtensorMap *m, const void *base, int H, bool fp8, uint64_t tokens = 1,
+                     uint32_t box_rows = bsa::kTile) {
   const cuuint64_t elem = fp8 ? 1 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)bsa::kHeadDim, (cuuint64_t)H, (cuuint64_t)tokens};
   cuuint64_t strides[2] = {bsa::kHeadDim * elem, (cuuint64_t)H * bsa::kHeadDim * elem};
-  cuuint32_t box[3] = {(cuuint32_t)(128 / elem), 1, (cuuint32_t)bsa::kTile};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / elem), 1, (cuuint32_t)box_rows};
   cuuint32_t estride[3] = {1, 1, 1};
   const CUresult r =
       g_encode(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
@@ -376,7 +377,10 @@ bsa_status_t bsa_block_importance(const void *q, const void *k, const int32_t *c
   if (!encoder()) return BSA_ERR_CUDA;
 
   CUtensorMap tmpl[2];
-  if (!encode_tile_map(&tmpl[0], q, Hq, false) || !encode_tile_map(&tmpl[1], k, Hkv, false))
+  // Q in 64-row boxes: a tile is one head's last 128 positions or the last
+  // 64 of two heads
+  if (!encode_tile_map(&tmpl[0], q, Hq, false, 1, bsa::kTile / 2) ||
+      !encode_tile_map(&tmpl[1], k, Hkv, false))
     return BSA_ERR_INVALID_ARG;
   Workspace *ws = nullptr;   // holds the status word
   if ((st = scratch_for(dev, stream, sizeof(Workspace), &ws)) != BSA_OK) return st;
@@ -406,6 +410,7 @@ bsa_status_t bsa_block_importance(const void *q, const void *k, const int32_t *c
   p.group = Hq / Hkv;
   p.n_window = n_window;
   p.causal = causal;
+  p.pair = (n_window <= bsa::kTile / 2 && p.group % 2 == 0) ? 2 : 1;
   p.c = (float)(1.0 / std::sqrt((double)d) * 1.4426950408889634);
   p.wait_limit_ns = t_wait_limit_ns;
   if (bsa::launch_importance(p, tmpl, info->sm_count, stream) != cudaSuccess) return BSA_ERR_CUDA;

@@ -17,7 +17,10 @@
 //    16-block chunk, query head), consecutive items = the query heads of one
 //    chunk, so the CTAs running together share K tiles through L2. The last
 //    128 query positions of the sequence are one Q tile (rows before the
-//    window are ignored); each key block is one K tile. S = Q K^T goes to one
+//    window are ignored); each key block is one K tile. For a window of at
+//    most 64 rows and an even group, an item takes two query heads of the
+//    group instead: the last 64 positions of each fill the tile's two halves,
+//    so every MMA row and every epilogue lane carries a window row. S = Q K^T goes to one
 //    of two TMEM buffers (128 columns each) while the epilogue reduces the
 //    other: per row, t = max(S c) and e = sum exp2(S c - t) over the keys the
 //    row may see, written to a [head][block][row] table.
@@ -63,8 +66,11 @@ enum : int {
 };
 
 struct Item {
-  int s, h, kvh, chunk, g0, g1, a, L;
+  int s, h, kvh, chunk, g0, g1, a, L;   // h: the item's (first) query head
 };
+
+// items per chunk of a sequence: its query heads, or pairs of them
+__device__ __forceinline__ int heads_per_chunk(const ImpParams &p) { return p.Hq / p.pair; }
 
 __device__ __forceinline__ void decode_item(const ImpParams &p, int item, Item &it) {
   int lo = 0, hi = p.n_seqs;   // largest s with item_off[s] <= item
@@ -73,10 +79,11 @@ __device__ __forceinline__ void decode_item(const ImpParams &p, int item, Item &
     if (p.item_off[mid] <= item) lo = mid; else hi = mid;
   }
   const int local = item - p.item_off[lo];
-  const int chunk = local / p.Hq;
+  const int hpc = heads_per_chunk(p);
+  const int chunk = local / hpc;
   it.s = lo;
   it.chunk = chunk;
-  it.h = local - chunk * p.Hq;
+  it.h = (local - chunk * hpc) * p.pair;
   it.kvh = it.h / p.group;
   it.a = p.cu[lo];
   it.L = p.cu[lo + 1] - it.a;
@@ -90,7 +97,7 @@ __device__ __forceinline__ void decode_item(const ImpParams &p, int item, Item &
 // ============================================================ prologue
 
 __global__ void __launch_bounds__(1024)
-imp_prologue_kernel(const int32_t *__restrict__ cu, int n_seqs, int Hq, int64_t total_blocks,
+imp_prologue_kernel(const int32_t *__restrict__ cu, int n_seqs, int hpc, int64_t total_blocks,
                     ImpWorkspace *iw, int64_t *blk_off, int32_t *item_off, Workspace *ws,
                     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk) {
   __shared__ int s_bad;
@@ -108,7 +115,7 @@ imp_prologue_kernel(const int32_t *__restrict__ cu, int n_seqs, int Hq, int64_t 
       item_off[s] = (int32_t)min(items, (long long)INT_MAX);
       const long long nb = (cu[s + 1] - cu[s] + kTile - 1) / kTile;
       blocks += nb;
-      items += (long long)Hq * ((nb + kImpChunk - 1) / kImpChunk);
+      items += (long long)hpc * ((nb + kImpChunk - 1) / kImpChunk);
     }
     blk_off[n_seqs] = blocks;
     item_off[n_seqs] = (int32_t)min(items, (long long)INT_MAX);
@@ -179,11 +186,20 @@ __global__ void __launch_bounds__(kImpThreads, 1) imp_tiles_kernel(const __grid_
           break;
         }
         mbar_expect_tx(&bar[I_QF + qb], kTileBytes);
-        // the window is the last 128 positions: rows before the sequence start
-        // (or before token 0: zero fill) are never used
-        for (int b = 0; b < 2; ++b)
-          tma_load_3d(sptr + SM_Q + qb * kTileBytes + b * kBoxBytes, tq, &bar[I_QF + qb], b * 64,
-                      it.h, it.a + it.L - kTile);
+        // 64-row boxes. One head: its last 128 positions (rows before the
+        // sequence start, or before token 0: zero fill, are never used). Two
+        // heads: the last 64 positions of each, head h in rows 0-63.
+        const int tok = it.a + it.L - kTile / 2;
+        for (int b = 0; b < 2; ++b) {
+          uint8_t *dst = sptr + SM_Q + qb * kTileBytes + b * kBoxBytes;
+          if (p.pair == 2) {
+            tma_load_3d(dst, tq, &bar[I_QF + qb], b * 64, it.h, tok);
+            tma_load_3d(dst + kBoxBytes / 2, tq, &bar[I_QF + qb], b * 64, it.h + 1, tok);
+          } else {
+            tma_load_3d(dst, tq, &bar[I_QF + qb], b * 64, it.h, tok - kTile / 2);
+            tma_load_3d(dst + kBoxBytes / 2, tq, &bar[I_QF + qb], b * 64, it.h, tok);
+          }
+        }
         q_last[qb] = (int)qi++;
         for (int g = it.g0; g < it.g1; ++g) {
           const uint32_t st = kc % kKStages;
@@ -256,10 +272,14 @@ __global__ void __launch_bounds__(kImpThreads, 1) imp_tiles_kernel(const __grid_
     for (int item = blockIdx.x; item < total && ok && !abort_sh; item += gridDim.x) {
       Item it;
       decode_item(p, item, it);
-      const int pos = it.L - kTile + row;                 // position of this window row
+      // this lane's query head and window row (row r of a head's table is
+      // position L - 128 + r)
+      const int hh = (p.pair == 2 && row >= kTile / 2) ? it.h + 1 : it.h;
+      const int wrow = p.pair == 2 ? kTile / 2 + (row & (kTile / 2 - 1)) : row;
+      const int pos = it.L - kTile + wrow;
       const int last_key = p.causal ? min(pos, it.L - 1) : it.L - 1;
-      float *tt = p.stat_t + ((int64_t)it.h * p.total_blocks + p.blk_off[it.s]) * kTile + row;
-      float *te = p.stat_e + ((int64_t)it.h * p.total_blocks + p.blk_off[it.s]) * kTile + row;
+      float *tt = p.stat_t + ((int64_t)hh * p.total_blocks + p.blk_off[it.s]) * kTile + wrow;
+      float *te = p.stat_e + ((int64_t)hh * p.total_blocks + p.blk_off[it.s]) * kTile + wrow;
       float cm = -INFINITY, cl = 0.f;   // (t, e) combined over this chunk
       for (int g = it.g0; g < it.g1; ++g) {
         const uint32_t sb = sc & 1;
@@ -318,7 +338,8 @@ __global__ void __launch_bounds__(kImpThreads, 1) imp_tiles_kernel(const __grid_
         }
       }
       if (!ok) break;
-      const int64_t ci = ((int64_t)it.h * p.max_chunks + p.item_off[it.s] / p.Hq + it.chunk) * kTile + row;
+      const int64_t ci =
+          ((int64_t)hh * p.max_chunks + p.item_off[it.s] / heads_per_chunk(p) + it.chunk) * kTile + wrow;
       p.chunk_m[ci] = cm;
       p.chunk_l[ci] = cl;
     }
@@ -349,7 +370,7 @@ __global__ void __launch_bounds__(kTile) imp_lse_kernel(const __grid_constant__ 
   }
   const int nch = ((L + kTile - 1) / kTile + kImpChunk - 1) / kImpChunk;
   const int ne = min(p.n_window, L);
-  const int64_t base = ((int64_t)h * p.max_chunks + p.item_off[s] / p.Hq) * kTile + r;
+  const int64_t base = ((int64_t)h * p.max_chunks + p.item_off[s] / heads_per_chunk(p)) * kTile + r;
   float m = -INFINITY, l = 0.f;
   for (int c0 = 0; c0 < nch; c0 += 8) {
     float cm[8], cl[8];
@@ -392,9 +413,9 @@ __global__ void __launch_bounds__(256) imp_block_kernel(const __grid_constant__ 
     const float *E = p.stat_e + ((int64_t)h * p.total_blocks + b) * kTile;
     float acc = 0.f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < 4; ++k) {   // window rows only: the others may never be written
       const int rr = lane + 32 * k;
-      acc += E[rr] * ex2_approx(T[rr] - lse[rr]);
+      if (rr >= kTile - ne) acc += E[rr] * ex2_approx(T[rr] - lse[rr]);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
@@ -550,7 +571,7 @@ size_t topp_smem_bytes() { return (size_t)kTopPMaxBlocks * 8; }
 
 cudaError_t launch_importance(const ImpParams &p, const CUtensorMap tmpl[2], int num_ctas,
                               cudaStream_t stream) {
-  imp_prologue_kernel<<<1, 1024, 0, stream>>>(p.cu, p.n_seqs, p.Hq, p.total_blocks, p.iw,
+  imp_prologue_kernel<<<1, 1024, 0, stream>>>(p.cu, p.n_seqs, p.Hq / p.pair, p.total_blocks, p.iw,
                                                const_cast<int64_t *>(p.blk_off),
                                                const_cast<int32_t *>(p.item_off), p.ws, tmpl[0],
                                                tmpl[1]);

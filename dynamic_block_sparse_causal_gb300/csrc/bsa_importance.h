@@ -19,7 +19,7 @@ constexpr int kTopPThreads = 1024;
 // Per-stream scratch of the importance path. Tables follow the header:
 //   int64 blk_off[n_seqs + 1]            first block of every sequence
 //   int32 item_off[n_seqs + 1]           first work item of every sequence
-//                                        (= Hq x first 16-block chunk)
+//                                        (= Hq / pair x first 16-block chunk)
 //   float stat_t[Hq][total_blocks][128]  per window row and key block:
 //   float stat_e[Hq][total_blocks][128]  t = max of S c, e = sum of exp2(S c - t)
 //   float chunk_m[Hq][chunks][128]       the same pair combined over a chunk
@@ -73,6 +73,7 @@ struct ImpParams {
   float *mean_scores;        // [total_blocks] or null
   int64_t total_blocks;
   int32_t n_seqs, Hq, Hkv, group, n_window, causal;
+  int32_t pair;              // query heads per work item: 2 for a window of <= 64 rows and an even group
   float c;                   // softmax scale * log2(e)
   uint64_t wait_limit_ns;
 };
