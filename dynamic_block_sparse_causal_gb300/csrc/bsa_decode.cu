@@ -30,6 +30,8 @@
 #include <climits>
 #include <cmath>
 
+#include <utility>
+
 #include "bsa_decode.h"
 #include "ptx.cuh"
 
@@ -91,6 +93,7 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 __global__ void __launch_bounds__(1024) dec_prologue_kernel(const __grid_constant__ DecParams p) {
   __shared__ int s_bad;
   const int tid = threadIdx.x;
+  grid_dep_launch();   // the score kernel may set up meanwhile; it waits for this grid
   if (tid == 0)
     s_bad = p.cu_q[0] != 0 || p.cu_k[0] != 0 || (int64_t)p.cu_k[p.n_seqs] != p.total_k;
   __syncthreads();
@@ -201,6 +204,8 @@ dec_scores_kernel(const __grid_constant__ DecParams p, const __grid_constant__ C
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_sh;
+  grid_dep_wait();     // tables of the previous kernel
+  grid_dep_launch();
   const int total = p.dw->total_items;
   const uint64_t limit = p.wait_limit_ns;
 
@@ -419,6 +424,8 @@ dec_pv_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUten
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_sh;
+  grid_dep_wait();     // tables of the previous kernel
+  grid_dep_launch();
   const int total = p.dw->total_items;
   const uint64_t limit = p.wait_limit_ns;
 
@@ -691,6 +698,7 @@ dec_pv_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUten
 __global__ void __launch_bounds__(4 * kTile) dec_combine_kernel(const __grid_constant__ DecParams p) {
   __shared__ float red[4 * kTile / 32];
   __shared__ float part[3][kTile], lpart[4];
+  grid_dep_wait();
   if (p.dw->total_items == 0) return;
   const int per_seq = p.max_q * p.Hq;
   const int s = blockIdx.x / per_seq, rem = blockIdx.x - s * per_seq;
@@ -749,26 +757,48 @@ size_t pv_smem_bytes(int RB) {
 }
 }  // namespace
 
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous one on the stream finishes, and waits for it in grid_dep_wait.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), int grid, int block, size_t smem,
+                             cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 cudaError_t launch_decode(const DecParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                           int sm_count, cudaStream_t stream) {
   const int64_t max_tiles = p.total_k / kTile + p.n_seqs;
   const int64_t max_items = (int64_t)p.Hkv * (max_tiles / p.split + p.n_seqs);
   const int grid = (int)(max_items < 4LL * sm_count ? max_items : 4LL * sm_count);
+  const int block = kDecScoreThreads + 64;
   dec_prologue_kernel<<<1, 1024, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   if (p.rows <= 16)
-    dec_scores_kernel<16><<<grid, kDecScoreThreads + 64, dec_smem_bytes(16), stream>>>(p, tk);
+    e = launch_dependent(dec_scores_kernel<16>, grid, block, dec_smem_bytes(16), stream, p, tk);
   else
-    dec_scores_kernel<32><<<grid, kDecScoreThreads + 64, dec_smem_bytes(32), stream>>>(p, tk);
+    e = launch_dependent(dec_scores_kernel<32>, grid, block, dec_smem_bytes(32), stream, p, tk);
+  if (e != cudaSuccess) return e;
   if (p.rows <= 4)
-    dec_pv_kernel<4><<<grid, kDecScoreThreads + 64, pv_smem_bytes(4), stream>>>(p, tv);
+    e = launch_dependent(dec_pv_kernel<4>, grid, block, pv_smem_bytes(4), stream, p, tv);
   else if (p.rows <= 8)
-    dec_pv_kernel<8><<<grid, kDecScoreThreads + 64, pv_smem_bytes(8), stream>>>(p, tv);
+    e = launch_dependent(dec_pv_kernel<8>, grid, block, pv_smem_bytes(8), stream, p, tv);
   else if (p.rows <= 16)
-    dec_pv_kernel<16><<<grid, kDecScoreThreads + 64, pv_smem_bytes(16), stream>>>(p, tv);
+    e = launch_dependent(dec_pv_kernel<16>, grid, block, pv_smem_bytes(16), stream, p, tv);
   else
-    dec_pv_kernel<32><<<grid, kDecScoreThreads + 64, pv_smem_bytes(32), stream>>>(p, tv);
-  dec_combine_kernel<<<p.n_seqs * p.max_q * p.Hq, 4 * kTile, 0, stream>>>(p);
-  return cudaGetLastError();
+    e = launch_dependent(dec_pv_kernel<32>, grid, block, pv_smem_bytes(32), stream, p, tv);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(dec_combine_kernel, p.n_seqs * p.max_q * p.Hq, 4 * kTile, 0, stream, p);
 }
 
 cudaError_t prepare_decode() {

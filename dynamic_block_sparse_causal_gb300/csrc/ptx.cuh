@@ -163,6 +163,16 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before the previous kernel on the stream has
+// finished; it calls grid_dep_wait() before touching anything that kernel
+// writes. grid_dep_launch() lets the next such kernel start once every CTA
+// of this grid has issued it (or exited).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
 // and stride byte offsets (all >> 4), descriptor version 1 at bit 46, layout
 // type at bits 61..63 (2 = 128-byte swizzle).
