@@ -30,8 +30,6 @@
 #include <climits>
 #include <cmath>
 
-#include <utility>
-
 #include "bsa_decode.h"
 #include "ptx.cuh"
 
@@ -756,24 +754,6 @@ size_t pv_smem_bytes(int RB) {
   return (size_t)kStages * (kTileBytes + RB * kTile * 4) + 1024 + 2 * (size_t)N * 256;
 }
 }  // namespace
-
-// Launch with programmatic stream serialisation: the kernel may start while
-// the previous one on the stream finishes, and waits for it in grid_dep_wait.
-template <typename... Params, typename... Args>
-cudaError_t launch_dependent(void (*kernel)(Params...), int grid, int block, size_t smem,
-                             cudaStream_t stream, Args &&...args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3((unsigned)block);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-}
 
 cudaError_t launch_decode(const DecParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                           int sm_count, cudaStream_t stream) {

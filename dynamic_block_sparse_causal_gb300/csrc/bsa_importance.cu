@@ -102,6 +102,7 @@ imp_prologue_kernel(const int32_t *__restrict__ cu, int n_seqs, int hpc, int64_t
                     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk) {
   __shared__ int s_bad;
   const int tid = threadIdx.x;
+  grid_dep_launch();   // the tile kernel may start; it waits for this grid
   if (tid == 0) s_bad = cu[0] != 0;
   __syncthreads();
   for (int s = tid; s < n_seqs; s += blockDim.x)
@@ -150,6 +151,8 @@ __global__ void __launch_bounds__(kImpThreads, 1) imp_tiles_kernel(const __grid_
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t *sptr = smem_raw + (sbase - raw);
+  grid_dep_wait();   // the prologue's tables and tensor maps
+  grid_dep_launch();
   const int total = p.iw->total_items;
   const uint64_t limit = p.wait_limit_ns;
 
@@ -359,6 +362,8 @@ __global__ void __launch_bounds__(kImpThreads, 1) imp_tiles_kernel(const __grid_
 // row's log2-sum-exp2 over the sequence's chunks. Rows before the window (or
 // without any key) get +inf, so that they weigh nothing below.
 __global__ void __launch_bounds__(kTile) imp_lse_kernel(const __grid_constant__ ImpParams p) {
+  grid_dep_wait();
+  grid_dep_launch();
   if (p.iw->total_items == 0) return;   // rejected, or nothing to do
   const int s = blockIdx.x / p.Hq, h = blockIdx.x - s * p.Hq;
   const int L = p.cu[s + 1] - p.cu[s];
@@ -395,6 +400,8 @@ __global__ void __launch_bounds__(kTile) imp_lse_kernel(const __grid_constant__ 
 // Per head, 32 consecutive blocks of the packed block axis per CTA, four per
 // warp: score = sum over window rows of e exp2(t - lse), divided by n G.
 __global__ void __launch_bounds__(256) imp_block_kernel(const __grid_constant__ ImpParams p) {
+  grid_dep_wait();
+  grid_dep_launch();
   if (p.iw->total_items == 0) return;
   const int h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -424,6 +431,7 @@ __global__ void __launch_bounds__(256) imp_block_kernel(const __grid_constant__ 
 }
 
 __global__ void imp_mean_kernel(const __grid_constant__ ImpParams p) {
+  grid_dep_wait();
   if (p.iw->total_items == 0) return;
   const float inv = 1.f / (float)p.Hq;
   for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < p.total_blocks;
@@ -575,14 +583,29 @@ cudaError_t launch_importance(const ImpParams &p, const CUtensorMap tmpl[2], int
                                                const_cast<int64_t *>(p.blk_off),
                                                const_cast<int32_t *>(p.item_off), p.ws, tmpl[0],
                                                tmpl[1]);
-  imp_tiles_kernel<<<num_ctas, kImpThreads, importance_smem_bytes(), stream>>>(p);
-  imp_lse_kernel<<<p.n_seqs * p.Hq, kTile, 0, stream>>>(p);
-  if (p.total_blocks > 0)
-    imp_block_kernel<<<dim3((unsigned)((p.total_blocks + 31) / 32), p.Hq), 256, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if ((e = launch_dependent(imp_tiles_kernel, num_ctas, kImpThreads, importance_smem_bytes(), stream,
+                            p)) != cudaSuccess)
+    return e;
+  if ((e = launch_dependent(imp_lse_kernel, p.n_seqs * p.Hq, kTile, 0, stream, p)) != cudaSuccess)
+    return e;
+  if (p.total_blocks > 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((p.total_blocks + 31) / 32), (unsigned)p.Hq);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, imp_block_kernel, p)) != cudaSuccess) return e;
+  }
   if (p.mean_scores && p.total_blocks > 0) {
     const int64_t want = (p.total_blocks + 255) / 256;
     const int grid = (int)(want < 4096 ? want : 4096);
-    imp_mean_kernel<<<grid, 256, 0, stream>>>(p);
+    if ((e = launch_dependent(imp_mean_kernel, grid, 256, 0, stream, p)) != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <utility>
 
 namespace bsa {
 
@@ -89,5 +90,23 @@ void current_fp8_scales(const float **q, const float **k, const float **v);
 // FP8 quantiser (bsa_quant.cu).
 cudaError_t launch_quantize_fp8(const void *x, int64_t tokens, int H, int d, uint8_t *codes,
                                 float *scale, cudaStream_t stream);
+
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous one on the stream finishes, and waits for it in grid_dep_wait.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), int grid, int block, size_t smem,
+                             cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace bsa
