@@ -38,3 +38,24 @@ def test_item_dense_flops_sums_to_layer():
     n = 16
     total = sum(bench.item_dense_flops(i) for i in range(n))
     assert total == bench.dense_flops([n * 128], 1)
+
+
+def test_reference_arm_prints_one_contract_line():
+    """The CPU reference arm (the oracle on a bounded sample) prints one JSON
+    line with the contract's keys; the small single-head layer keeps it quick."""
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--config", "C0", "--steps", "1", "--warmup", "0", "--ref-budget", "0.5"],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [x for x in r.stdout.splitlines() if x.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e", "impl"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
