@@ -23,8 +23,8 @@ pytestmark = pytest.mark.gpu
 
 
 @functools.lru_cache(maxsize=2)
-def problem(name):
-    return gi.config(name)
+def problem(name, sink=4.0):
+    return gi.config(name, sink=sink)
 
 
 def whole_output_properties(p, g):
@@ -61,3 +61,17 @@ def test_lambda_monotone_on_full_layer():
     hi = _gpu.run(p, lam=5e-2)["bitmap"]
     assert np.count_nonzero(lo & ~hi) == 0
     assert np.unpackbits(hi.view(np.uint8)).sum() >= np.unpackbits(lo.view(np.uint8)).sum()
+
+
+def test_full_size_weak_sink_sampled():
+    """The 32K layer with the sink at 0.25 u (the bench's diagnostic): about
+    two thirds of the tiles skipped, so kept and skipped tiles interleave at
+    full size."""
+    p = problem("C1", 0.25)
+    g = _gpu.run(p, lam=0.01)
+    whole_output_properties(p, g)
+    bits = np.unpackbits(g["bitmap"].view(np.uint8)).sum()
+    frac = bits / (p.Hq * layout.tiles(p.seqlens[0]) * (layout.tiles(p.seqlens[0]) + 1) // 2)
+    assert 0.5 < frac < 0.8, frac
+    r = _gpu.compare(p, g, items=_gpu.sample_items(p, 16, seed=2))
+    print("weak sink", frac, r)
