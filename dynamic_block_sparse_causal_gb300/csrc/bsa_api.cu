@@ -335,6 +335,7 @@ bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
   p.c = (float)(1.0 / std::sqrt((double)d) * 1.4426950408889634);
   p.log2_lambda = lambda > 0.f ? (float)std::log2((double)lambda) : -INFINITY;
   p.wait_limit_ns = t_wait_limit_ns;
+  p.debug_drop_k_load = t_drop_k_load;
   if (bsa::launch_decode(p, tk, tv, info->sm_count, stream) != cudaSuccess) return BSA_ERR_CUDA;
   return BSA_OK;
 }
@@ -413,6 +414,7 @@ bsa_status_t bsa_block_importance(const void *q, const void *k, const int32_t *c
   p.pair = (n_window <= bsa::kTile / 2 && p.group % 2 == 0) ? 2 : 1;
   p.c = (float)(1.0 / std::sqrt((double)d) * 1.4426950408889634);
   p.wait_limit_ns = t_wait_limit_ns;
+  p.debug_drop_k_load = t_drop_k_load;
   if (bsa::launch_importance(p, tmpl, info->sm_count, stream) != cudaSuccess) return BSA_ERR_CUDA;
   return BSA_OK;
 }

@@ -219,8 +219,10 @@ dec_scores_kernel(const __grid_constant__ DecParams p, const __grid_constant__ C
         for (int j = it.j0; j < it.j1; ++j, ++kc) {
           const uint32_t b = kc % kStages;
           if (!(ok = mbar_wait(&kempty[b], ((kc / kStages) & 1) ^ 1, limit))) break;
-          load_tile(ring + b * kTileBytes, &tk, &kfull[b], it.kvh, it.ak + j * kTile);
-          last_issue[b] = (int)kc;
+          if ((int)kc != p.debug_drop_k_load) {
+            load_tile(ring + b * kTileBytes, &tk, &kfull[b], it.kvh, it.ak + j * kTile);
+            last_issue[b] = (int)kc;
+          }
         }
       }
       if (!ok) abort_sh = 1;

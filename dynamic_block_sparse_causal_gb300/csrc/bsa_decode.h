@@ -82,6 +82,7 @@ struct DecParams {
   int32_t split;              // key tiles per split: 8 or 16
   float c, log2_lambda;
   uint64_t wait_limit_ns;
+  int32_t debug_drop_k_load;  // >= 0: the score producer omits that K load (fault drill)
 };
 
 cudaError_t launch_decode(const DecParams &p, const CUtensorMap &tk, const CUtensorMap &tv,

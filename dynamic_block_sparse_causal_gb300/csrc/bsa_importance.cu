@@ -210,11 +210,14 @@ __global__ void __launch_bounds__(kImpThreads, 1) imp_tiles_kernel(const __grid_
             abort_sh = 1;
             break;
           }
-          mbar_expect_tx(&bar[I_KF + st], kTileBytes);
-          for (int b = 0; b < 2; ++b)
-            tma_load_3d(sptr + SM_K + st * kTileBytes + b * kBoxBytes, tk, &bar[I_KF + st],
-                        b * 64, it.kvh, it.a + g * kTile);
-          k_last[st] = (int)kc++;
+          if ((int)kc != p.debug_drop_k_load) {
+            mbar_expect_tx(&bar[I_KF + st], kTileBytes);
+            for (int b = 0; b < 2; ++b)
+              tma_load_3d(sptr + SM_K + st * kTileBytes + b * kBoxBytes, tk, &bar[I_KF + st],
+                          b * 64, it.kvh, it.a + g * kTile);
+            k_last[st] = (int)kc;
+          }
+          ++kc;
         }
       }
       if (abort_sh) {   // bounded wait for this CTA's copies still in flight

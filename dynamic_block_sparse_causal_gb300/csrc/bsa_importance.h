@@ -76,6 +76,7 @@ struct ImpParams {
   int32_t pair;              // query heads per work item: 2 for a window of <= 64 rows and an even group
   float c;                   // softmax scale * log2(e)
   uint64_t wait_limit_ns;
+  int32_t debug_drop_k_load;  // >= 0: the tile producer omits that K load (fault drill)
 };
 
 // Prologue, score tiles, per-head reduction and head mean, in stream order.

@@ -336,13 +336,17 @@ bsa_status_t bsa_get_device_status(bsa_stream_t stream);
 
 /*
  * Fault drill, for tests of the failure path only. For the calling host
- * thread, later bsa_prefill_fwd calls bound every device pipeline wait by
- * wait_limit_ns, and, when drop_k_load >= 0, the TMA producer of every CTA
- * leaves out its drop_k_load-th K tile load so that the MMA warp's wait for
- * it runs out. The kernel then records BSA_ERR_TIMEOUT (read it with
- * bsa_get_device_status), waits with the same bound for the copies and MMAs
- * it has in flight, frees its tensor memory and returns; the context stays
- * usable. bsa_debug_fault_drill(-1, 2000000000) restores the defaults.
+ * thread, later bsa_prefill_fwd*, bsa_decode_fwd and bsa_block_importance
+ * calls bound every device pipeline wait by wait_limit_ns, and, when
+ * drop_k_load >= 0, the K-tile TMA producer of every CTA (of the forward,
+ * decode score or importance score kernel) leaves out its drop_k_load-th K
+ * tile load so that the MMA warp's wait for it runs out. The kernel then
+ * records BSA_ERR_TIMEOUT (read it with bsa_get_device_status), waits with
+ * the same bound for the copies and MMAs it has in flight, frees its tensor
+ * memory and returns; the kernels after it in the same call run on whatever
+ * the tables hold (the result is meaningless, the status says so) and the
+ * context stays usable. bsa_debug_fault_drill(-1, 2000000000) restores the
+ * defaults.
  */
 bsa_status_t bsa_debug_fault_drill(int32_t drop_k_load, int64_t wait_limit_ns);
 

@@ -5,7 +5,8 @@
 * the fault drill drops one K tile load per CTA and bounds every pipeline
   wait to 100 ms: the MMA warp's wait runs out, the kernel records
   BSA_ERR_TIMEOUT, drains its own copies and MMAs, frees tensor memory and
-  returns; the next normal call on the same context is correct.
+  returns; the next normal call on the same context is correct. The decode
+  and block-importance score kernels take the same drill.
 """
 from __future__ import annotations
 
@@ -59,3 +60,31 @@ def _drill_args(p):
     bm = torch.empty((b.skip_bitmap_words(p.cu_seqlens, p.Hq),), dtype=torch.int32, device="cuda")
     _keep[:] = [q, k, v, cu, out, lse, bm]
     return (q, k, v, cu, p.n_seqs, p.Hq, p.Hkv, p.d, 1, 0.01, b.BSA_BF16, out, lse, bm)
+
+
+def test_fault_drill_in_decode_and_importance():
+    """The same drill in the split-KV decode score kernel and the importance
+    score kernel: each CTA's first K load is left out, the call records
+    BSA_ERR_TIMEOUT, and the next normal calls are correct."""
+    import test_gpu_decode as td
+    import test_gpu_importance as ti
+    from gen import inputs as gi
+    from oracle import importance as imp
+    b = _gpu.bsa()
+    base = _cases.small_problem("gqa4")
+    pd = gi.chunk(base, [2, 1])
+    try:
+        b.check(b.debug_fault_drill(0, 100_000_000), "drill")
+        _, st = td.run_decode(pd, 0.005)
+        assert st == 4   # BSA_ERR_TIMEOUT (run_decode reads and clears the status)
+        _, _, st = ti.run_importance(base, 64)
+        assert st == 4
+    finally:
+        b.check(b.debug_fault_drill(-1, 2_000_000_000), "restore")
+    g, st = td.run_decode(pd, 0.005)
+    assert st == 0
+    _gpu.compare(pd, g)
+    sc, mn, st = ti.run_importance(base, 64)
+    assert st == 0
+    ti.check_scores(sc.cpu().numpy(),
+                    imp.block_importance(base.q, base.k, base.cu_seqlens, base.Hq, base.Hkv, 64, True))
