@@ -356,6 +356,8 @@ def gpu_arm(args, rank, world, local_rank):
                 "algorithmic_bytes": int(2 * (p.q.size + p.k.size + p.v.size + p.q.size) + 4 * Hq * T),
                 "peak_source": "MEASURED_PEAKS.json bf16_tflops (burst)" if "bf16_tflops" in peaks
                 else "fallback 1900 TFLOP/s", "flops_per_launch": xflops}
+    if "bf16_tflops_sustained" in peaks:   # the same work against the seconds-long cuBLAS rate
+        roofline["frac_of_sustained"] = round(achieved / peaks["bf16_tflops_sustained"], 4)
 
     # lambda sweep on the same layer (skip fraction and TFLOP/s for each lambda)
     sweep = []
