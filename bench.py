@@ -66,10 +66,11 @@ def popcount(words: np.ndarray) -> int:
 
 # ------------------------------------------------------------------ measured DRAM traffic
 
-KERNEL_SOURCES = ("dynamic_block_sparse_causal_gb300/csrc/bsa_fwd.cu",
+KERNEL_SOURCES = ("dynamic_block_sparse_causal_gb300/csrc/bsa_skip.cu",
+                  "dynamic_block_sparse_causal_gb300/csrc/bsa_tile.cuh",
                   "dynamic_block_sparse_causal_gb300/csrc/ptx.cuh",
                   "dynamic_block_sparse_causal_gb300/csrc/bsa_internal.h")
-DRAM_PROFILE = os.path.join(ROOT, "profiles", "fwd_kernel_c2_dram.md")
+DRAM_PROFILE = os.path.join(ROOT, "profiles", "skip_kernel_c2_dram.md")
 
 
 def kernel_sources_sha256() -> str:

@@ -18,8 +18,8 @@ LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libbsa.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["bsa_api.cu", "bsa_fwd.cu", "bsa_quant.cu", "bsa_noalloc.cu", "bsa_importance.cu",
-           "bsa_decode.cu"]
+SOURCES = ["bsa_api.cu", "bsa_fwd.cu", "bsa_skip.cu", "bsa_quant.cu", "bsa_noalloc.cu",
+           "bsa_importance.cu", "bsa_decode.cu"]
 
 
 def nvcc() -> str:

@@ -75,8 +75,8 @@ bsa_status_t device_info(int dev, DeviceInfo **out) {
       return BSA_ERR_CUDA;
     d.supported = (major == 10 && minor == 3);
     if (d.supported &&
-        (bsa::prepare_forward() != cudaSuccess || bsa::prepare_importance() != cudaSuccess ||
-         bsa::prepare_decode() != cudaSuccess))
+        (bsa::prepare_forward() != cudaSuccess || bsa::prepare_skip() != cudaSuccess ||
+         bsa::prepare_importance() != cudaSuccess || bsa::prepare_decode() != cudaSuccess))
       return BSA_ERR_CUDA;
     d.ready = true;
   }
@@ -219,7 +219,10 @@ bsa_status_t prefill(const void *q, const void *k, const void *v, const int32_t 
   p.log2_lambda = lambda > 0.f ? (float)std::log2((double)lambda) : -INFINITY;
   p.wait_limit_ns = t_wait_limit_ns;
   p.debug_drop_k_load = t_drop_k_load;
-  if (bsa::launch_forward(p, fp8, info->sm_count, stream) != cudaSuccess) return BSA_ERR_CUDA;
+  // lambda > 0: decisions first, then the kept tiles; lambda = 0: one dense pass
+  const cudaError_t e = lambda > 0.f ? bsa::launch_skip(p, fp8, info->sm_count, stream)
+                                     : bsa::launch_forward(p, fp8, info->sm_count, stream);
+  if (e != cudaSuccess) return BSA_ERR_CUDA;
   return BSA_OK;
 }
 

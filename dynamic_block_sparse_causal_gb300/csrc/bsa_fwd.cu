@@ -1,23 +1,21 @@
-// Block-skipping causal prefill attention: device code for sm_103a.
+// Causal prefill attention, device code for sm_103a: the per-call prologue
+// and the dense forward kernel (lambda = 0; the skipping kernel for
+// lambda > 0 is in bsa_skip.cu).
 //
 // Operation: dynamic sparse attention deployment guide
 // ("长上下文推理加速方案部署实战：基于动态稀疏注意力机制的推理服务优化指南"),
-// §3.2 -- online softmax over key blocks in order; a block whose local max
-// score falls below the running max by more than the threshold skips the
-// exponentials, its V load and its P.V product. Threshold read as
-// tile_max < running_max + ln(lambda) per row, AND-ed over the 128 rows of
-// the query tile (§3.3 and §6.1 fix the direction: larger lambda prunes more).
+// §3.2 -- online softmax over key blocks in order; with lambda = 0 the skip
+// rule never fires and the pass is exact dense causal attention.
 //
 // Two kernels:
 //  * prologue_kernel (1 CTA): validates cu_seqlens, orders sequences longest
 //    first, builds the work-item level table and the skip-bitmap offsets,
-//    and writes the TMA tensor maps with the token extent patched in.
-//  * fwd_kernel<FP8, SKIP> (persistent, one CTA per SM, 384 threads):
-//      warp 0  lane 0   TMA producer: Q tiles, the K ring (4 stages with
-//                       skipping on, 3 with it off), and, when skipping is off,
-//                       V with every K (2-stage ring)
-//      warp 1  lane 0   tcgen05 MMA issuer; with skipping on it also requests
-//                       V_j (one stage) as soon as a query tile votes to keep j
+//    and writes the TMA tensor maps with the token extent patched in. Both
+//    forward kernels consume its tables.
+//  * fwd_kernel<FP8> (persistent, one CTA per SM, 384 threads):
+//      warp 0  lane 0   TMA producer: Q tiles, the K ring (3 stages) and V
+//                       with every K (2-stage ring)
+//      warp 1  lane 0   tcgen05 MMA issuer
 //      warp 2  lane 0   fetches the next work item (atomic counter)
 //      warps 4-7        softmax warpgroup of query slot 0 (TMEM lanes 0-127)
 //      warps 8-11       softmax warpgroup of query slot 1
@@ -28,8 +26,7 @@
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512),
 // fp32, lane = query row; P_s (bf16 / e4m3) is written over the first
 // columns of S_s and read from there by the P.V MMA. Shared memory
-// (1024-aligned, 128-byte swizzle), 32 KiB regions: Q0 Q1, then K[4] V[1]
-// with skipping on or K[3] V[2] with it off.
+// (1024-aligned, 128-byte swizzle), 32 KiB regions: Q0 Q1, K[3], V[2].
 //
 // Pipeline counters live in registers within a work item and in shared
 // memory between items, one set per role, so that no role's registers carry
@@ -37,13 +34,12 @@
 // softmax warpgroups sets the length of the per-tile chain).
 //
 // Per key tile j and query slot s the softmax warpgroup loads S_s from TMEM,
-// masks the diagonal / tail, takes the row max, and votes with one
-// bar.red.and. The vote is posted at once: a skipped tile frees S_s for the
-// next QK^T; a kept tile lets the MMA warp request V_j while the warpgroup
-// computes P = exp2(S c - m_ref) (lazy O rescale when the reference max
-// grows by more than 2^8) into TMEM and then posts P-ready. The MMA warp
-// issues O_s += P_s V_j before the next S_s, so the tensor pipe's in-order
-// execution protects P until it has been read.
+// masks the diagonal / tail and computes P = exp2(S c - m_ref) into TMEM:
+// on the first tile after the row max, later in one pass against the current
+// reference, with a lazy O rescale (and a second pass) only for a row whose
+// max grows by more than 2^8; then it posts P-ready. The MMA warp issues
+// O_s += P_s V_j before the next S_s, so the tensor pipe's in-order execution
+// protects P until it has been read.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -52,8 +48,11 @@
 
 #include "bsa_internal.h"
 #include "ptx.cuh"
+#include "bsa_tile.cuh"
 
 namespace bsa {
+
+using namespace tile;
 
 // ============================================================ prologue
 
@@ -80,7 +79,9 @@ prologue_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ cuk,
     const int Lq = cu[s + 1] - cu[s], Lk = cuk[s + 1] - cuk[s];
     // queries are the last Lq positions of a sequence of Lk keys
     if (Lq < 0 || Lk < 0 || (causal && Lk < Lq) || (Lq > 0 && Lk == 0)) atomicOr(&s_bad, 1);
-    atomicMax(&s_maxn, (Lq + kTile - 1) / kTile);
+    // query and key tiles per sequence are bounded by the level table and the
+    // skipping kernel's on-chip keep bits (one per key tile)
+    atomicMax(&s_maxn, max((Lq + kTile - 1) / kTile, (Lk + kTile - 1) / kTile));
     if (page_table && Lk > 0) {   // every page a sequence reads must exist
       const int nk = (Lk + kTile - 1) / kTile;
       if (nk > max_pages) {
@@ -173,19 +174,11 @@ cudaError_t launch_prologue(const int32_t *cu_seqlens, const int32_t *cu_seqlens
 
 namespace {
 
-constexpr uint32_t kRegion = 32768;   // one bf16 tile slot in shared memory
-constexpr uint32_t kBox = 16384;      // one 128-row x 128-byte TMA box
 // K and V rings share five 32 KiB regions after the two Q tiles: 3 K + 2 V
-// stages with skipping off (V streams with every K), 4 K + 1 V with it on
-// (V is loaded only for kept tiles, K for every tile)
-constexpr int kKStages = 4, kVStages = 2;   // the deeper of the two, for barrier slots
-template <bool SKIP>
-struct Ring {
-  static constexpr int K = SKIP ? 4 : 3, V = SKIP ? 1 : 2;
-};
+// stages (V streams with every K)
+constexpr int KST = 3, VST = 2;
 constexpr uint32_t SM_Q0 = 0, SM_Q1 = kRegion, SM_K = 2 * kRegion, SM_BYTES = SM_K + 5 * kRegion;
 constexpr float kRescaleLog2 = 8.0f;  // lazy O rescale once m grows by 2^8
-constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kColS = 0, kColO = 256;   // TMEM: S_s at s*128, O_s at 256 + s*128
 // warp roles: TMA producer, MMA issuer, item fetch, then (from warp 4) the
 // softmax warpgroups of query slots 0 and 1 (warp w reaches TMEM lanes 32 (w % 4) ..)
@@ -195,118 +188,15 @@ constexpr int kWarpProd = 0, kWarpMma = 1, kWarpFetch = 2, kWarpSoftmax = 4;
 enum : int {
   B_Q = 0,
   B_KF = 1,
-  B_KE = B_KF + kKStages,
-  B_VF = B_KE + kKStages,
-  B_VE = B_VF + kVStages,
-  B_SF = B_VE + kVStages,   // S_s computed (per slot)
-  B_VOTE = B_SF + 2,        // slot s voted on the tile (S_s free if skipped)
-  B_PRDY = B_VOTE + 2,      // P_s written to TMEM (S_s consumed)
+  B_KE = B_KF + KST,
+  B_VF = B_KE + KST,
+  B_VE = B_VF + VST,
+  B_SF = B_VE + VST,        // S_s computed (per slot)
+  B_PRDY = B_SF + 2,        // P_s written to TMEM (S_s consumed)
   B_PV = B_PRDY + 2,        // O_s += P_s V done
   B_DRAIN = B_PV + 2,
   B_COUNT
 };
-
-template <bool FP8>
-struct Cfg {
-  static constexpr uint32_t kTileBytes = FP8 ? 16384 : 32768;
-  static constexpr int kBoxCols = FP8 ? 128 : 64;   // elements per 128-byte row
-  static constexpr int kBoxes = FP8 ? 1 : 2;        // boxes along the head dim
-  static constexpr int kSteps = FP8 ? 4 : 8;        // MMA K steps over 128
-  static constexpr uint32_t kIdescQK = IDesc<FP8 ? 0 : 1, false, 128, 128>::value;
-  static constexpr uint32_t kIdescPV = IDesc<FP8 ? 0 : 1, true, 128, 128>::value;
-};
-
-// S = Q K^T: A = Q (K-major), B = K (K-major), both 128-byte swizzled; each
-// K step advances 32 bytes inside the swizzle atom.
-template <bool FP8>
-__device__ __forceinline__ void issue_qk(uint32_t d, uint32_t qs, uint32_t ks) {
-#pragma unroll
-  for (int kk = 0; kk < Cfg<FP8>::kSteps; ++kk) {
-    const uint32_t off = FP8 ? kk * 32 : (kk >> 2) * kBox + (kk & 3) * 32;
-    const uint64_t a = sdesc_sw128(qs + off, 16, 1024);
-    const uint64_t b = sdesc_sw128(ks + off, 16, 1024);
-    if (FP8)
-      mma_f8_ss(d, a, b, Cfg<FP8>::kIdescQK, kk > 0);
-    else
-      mma_f16_ss(d, a, b, Cfg<FP8>::kIdescQK, kk > 0);
-  }
-}
-
-// O += P V: A = P from TMEM (row = lane, two bf16 or four e4m3 keys per
-// 32-bit column, so every K step is 8 columns), B = V as stored (keys x head
-// dim, head dim contiguous) = MN-major; 8-row key groups 1024 bytes apart,
-// the two 64-column halves of a bf16 V tile 16 KiB apart.
-template <bool FP8>
-__device__ __forceinline__ void issue_pv(uint32_t d, uint32_t p_tmem, uint32_t vs, bool acc) {
-#pragma unroll
-  for (int kk = 0; kk < Cfg<FP8>::kSteps; ++kk) {
-    const uint32_t boff = FP8 ? kk * 4096 : kk * 2048;
-    const uint64_t b = sdesc_sw128(vs + boff, kBox, 1024);
-    if (FP8)
-      mma_f8_ts(d, p_tmem + kk * 8, b, Cfg<FP8>::kIdescPV, (kk > 0 || acc) ? 1u : 0u);
-    else
-      mma_f16_ts(d, p_tmem + kk * 8, b, Cfg<FP8>::kIdescPV, (kk > 0 || acc) ? 1u : 0u);
-  }
-}
-
-__device__ void fetch_item(const FwdParams &p, int total_items, int maxn, int *dst) {
-  const int k = atomicAdd(&p.ws->counter, 1);
-  if (k >= total_items) {
-    dst[0] = 0;
-    return;
-  }
-  // KV head major: items [g * per_head, (g + 1) * per_head) belong to head g
-  const int per_head = total_items / p.Hkv;
-  const int kvh = k / per_head;
-  const int kr = k - kvh * per_head;
-  int lo = 0, hi = maxn - 1;   // smallest level whose first item is <= kr
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (p.level_start[mid] <= kr)
-      hi = mid;
-    else
-      lo = mid + 1;
-  }
-  const int U = p.pairs_per_group;
-  const int r = kr - p.level_start[lo];
-  const int s = p.seq_sorted[r / U];
-  const int pp = r % U;
-  const int h0 = kvh * p.group + 2 * pp;
-  const int a = p.cu_seqlens[s], ak = p.cu_seqlens_k[s];
-  dst[0] = 1;
-  dst[1] = s;
-  dst[2] = kvh;
-  dst[3] = h0;
-  dst[4] = (2 * pp + 1 < p.group) ? h0 + 1 : -1;
-  dst[5] = lo;
-  dst[6] = a;
-  dst[7] = p.cu_seqlens[s + 1] - a;
-  dst[8] = ak;
-  dst[9] = p.cu_seqlens_k[s + 1] - ak;
-}
-
-// 32 lanes x 64 consecutive 32-bit columns in one load (two 32-register halves).
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&a)[32], uint32_t (&b)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
-      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]),
-        "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]), "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]), "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31])
-      : "r"(taddr));
-}
-
-// Running row max over two 32-register chunks (three-input max, eight
-// independent chains).
-__device__ __forceinline__ void row_max64(float (&a)[8], const uint32_t (&v0)[32],
-                                          const uint32_t (&v1)[32]) {
-#pragma unroll
-  for (int i = 0; i < 32; i += 16) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      a[k] = max3f(a[k], __uint_as_float(v0[i + 2 * k]), __uint_as_float(v0[i + 2 * k + 1]));
-      a[k] = max3f(a[k], __uint_as_float(v1[i + 2 * k]), __uint_as_float(v1[i + 2 * k + 1]));
-    }
-  }
-}
 
 // 2^x on the FMA pipe, used for part of the exponentials so that they do not
 // all queue on the MUFU unit. Cody-Waite reduction to the nearest integer n
@@ -351,44 +241,25 @@ constexpr int kSpinSoftmax = BSA_SPIN_SOFTMAX;
 #endif
 constexpr int kFmaExpEvery = BSA_FMA_EXP_EVERY;
 
-// -inf on the masked columns of one 32-column chunk: keys past the query
-// (row r of the query tile sees columns up to r + doff of this key tile) or
-// past the end of the keys (tail tile, non-causal).
-__device__ __forceinline__ void mask_chunk(uint32_t (&v)[32], int ch, bool diag, bool tailt,
-                                           int row, int doff, int key0, int Lk) {
-#pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    const int col = ch * 32 + e;
-    if ((diag && col > row + doff) || (tailt && key0 + col >= Lk))
-      v[e] = __float_as_uint(-INFINITY);
-  }
-}
-
 }  // namespace
 
-// SKIP: the skip rule is on (lambda > 0). Each mode is its own instantiation,
-// so the code generated for one carries no branch of the other.
-template <bool FP8, bool SKIP>
+template <bool FP8>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = Cfg<FP8>;
-  constexpr int KST = Ring<SKIP>::K, VST = Ring<SKIP>::V;
   constexpr uint32_t SM_V = SM_K + KST * kRegion;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar[B_COUNT];
   __shared__ uint32_t tmem_sh;
   __shared__ int item_sh[2][10];
-  // keep_sh[s][j & 1] != 0: some row of slot s keeps key tile j (one bit per warp
-  // that keeps it); the MMA warp reads it after the slot's four vote arrivals
-  __shared__ volatile uint32_t keep_sh[2][2];
   __shared__ volatile int abort_sh;
   // last load issued into each K stage, V stage and the Q slot (-1: none), for
   // the bounded drain after a time-out
-  __shared__ int kc_last[kKStages], vc_last[kVStages], qc_last;   // sized for the deeper ring
+  __shared__ int kc_last[KST], vc_last[VST], qc_last;
   // Pipeline counters, persistent across items: each role keeps its own here
   // between items and in registers within one, so that no role carries another
   // role's counters in its registers.
   //   [0, 3)    producer: Q, K, V loads
-  //   [3, 9)    MMA warp: Q, K, V, votes of slots 0 / 1, P-ready of slots 0 / 1
+  //   [3, 6), [8, 10)  MMA warp: Q, K, V, P-ready of slots 0 / 1
   //   [12 + 4 s, 14 + 4 s)  softmax slot s: S tiles, P.V waits
   __shared__ uint32_t ctr_sh[20];
 
@@ -398,12 +269,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   uint8_t *sptr = smem_raw + (sbase - raw);
   Workspace *ws = p.ws;
   const uint64_t limit = p.wait_limit_ns;
-  constexpr bool v_prefetch = !SKIP;   // no skipping: V streams with K
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < B_COUNT; ++b)
-      mbar_init(&bar[b], (b == B_VOTE || b == B_VOTE + 1) ? 4 : 1);   // a vote: one arrival per warp
-    keep_sh[0][0] = keep_sh[0][1] = keep_sh[1][0] = keep_sh[1][1] = 0u;
+    for (int b = 0; b < B_COUNT; ++b) mbar_init(&bar[b], 1);
     fence_mbar_init();
     abort_sh = 0;
     for (int k = 0; k < 20; ++k) ctr_sh[k] = 0u;
@@ -469,17 +337,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             kc_last[st] = (int)kc;
           }
           ++kc;
-          if (v_prefetch) {
-            const uint32_t vs = vc % VST;
-            ok = mbar_wait(&bar[B_VE + vs], ((vc / VST) & 1) ^ 1, limit, kSpinIssuer);
-            if (!ok) break;
-            mbar_expect_tx(&bar[B_VF + vs], C::kTileBytes);
-            for (int b = 0; b < C::kBoxes; ++b)
-              tma_load_3d(sptr + SM_V + vs * kRegion + b * kBox, tv, &bar[B_VF + vs],
-                          b * C::kBoxCols, kvh, kv_row(j));
-            vc_last[vs] = (int)vc;
-            ++vc;
-          }
+          const uint32_t vs = vc % VST;   // V streams with K: every tile is kept
+          ok = mbar_wait(&bar[B_VE + vs], ((vc / VST) & 1) ^ 1, limit, kSpinIssuer);
+          if (!ok) break;
+          mbar_expect_tx(&bar[B_VF + vs], C::kTileBytes);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(sptr + SM_V + vs * kRegion + b * kBox, tv, &bar[B_VF + vs],
+                        b * C::kBoxCols, kvh, kv_row(j));
+          vc_last[vs] = (int)vc;
+          ++vc;
         }
         ctr_sh[0] = qc;
         ctr_sh[1] = kc;
@@ -489,27 +355,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       if (lane == 0) {
         // ------------------------------------------------ MMA issuer
         uint32_t qc = ctr_sh[3], kc = ctr_sh[4], vc = ctr_sh[5];
-        uint32_t vt0 = ctr_sh[6], vt1 = ctr_sh[7], pr0 = ctr_sh[8], pr1 = ctr_sh[9];
-        const void *tv = &ws->tmap[2];
+        uint32_t pr0 = ctr_sh[8], pr1 = ctr_sh[9];
         const uint32_t S0 = tmem + kColS, S1 = tmem + kColS + 128;
         const uint32_t O0 = tmem + kColO, O1 = tmem + kColO + 128;
         const uint32_t q0s = sbase + SM_Q0, q1s = sbase + SM_Q1;
-        // V_j request from this thread (skipping on): only kept tiles are loaded
-        auto issue_v = [&](int j) -> bool {
-          const uint32_t vs = vc % VST;
-          if (!mbar_wait(&bar[B_VE + vs], ((vc / VST) & 1) ^ 1, limit, kSpinIssuer)) return false;
-          mbar_expect_tx(&bar[B_VF + vs], C::kTileBytes);
-          for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(sptr + SM_V + vs * kRegion + b * kBox, tv, &bar[B_VF + vs],
-                        b * C::kBoxCols, kvh, kv_row(j));
-          vc_last[vs] = (int)vc;
-          return true;
-        };
         do {
-          // no vote of this item is in flight yet (the item started after a CTA barrier)
-          keep_sh[0][0] = keep_sh[0][1] = keep_sh[1][0] = keep_sh[1][1] = 0u;
-          // key tile 0 is never skipped: request its V before anything else
-          if (!v_prefetch && !(ok = issue_v(0))) break;
           ok = mbar_wait(&bar[B_Q], qc & 1, limit, kSpinIssuer);
           ++qc;
           if (!ok) break;
@@ -528,8 +378,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           ++kc;
           bool oinit0 = false, oinit1 = false;
           for (int j = 0; j <= last && ok; ++j) {
-            bool vload = v_prefetch || j == 0;   // V_j requested
-            bool vready = false;                 // V_j landed (waited)
+            bool vready = false;   // V_j landed (waited)
             const uint32_t vs = vc % VST;
             auto wait_v = [&]() -> bool {
               if (vready) return true;
@@ -538,18 +387,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
               vready = true;
               return true;
             };
-            // ---- slot 0: vote, then P.V (if kept) before the next S overwrites P
-            bool keep0 = true;   // with skipping off every tile is kept
-            if (!v_prefetch) {
-              ok = mbar_wait(&bar[B_VOTE + 0], vt0 & 1, limit, kSpinIssuer);
-              ++vt0;
-              if (!ok) break;
-              keep0 = keep_sh[0][j & 1] != 0;
-              keep_sh[0][(j + 1) & 1] = 0u;   // tile j - 1's entry: read, and reused by j + 1
-            }
-            if (keep0) {
-              if (!vload && !(ok = issue_v(j))) break;
-              vload = true;
+            // ---- slot 0: P.V before the next S overwrites P
+            {
               ok = mbar_wait(&bar[B_PRDY + 0], pr0 & 1, limit, kSpinIssuer);
               ++pr0;
               if (!ok || !(ok = wait_v())) break;
@@ -569,17 +408,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             }
             // ---- slot 1
             if (has1) {
-              bool keep1 = true;
-              if (!v_prefetch) {
-                ok = mbar_wait(&bar[B_VOTE + 1], vt1 & 1, limit, kSpinIssuer);
-                ++vt1;
-                if (!ok) break;
-                keep1 = keep_sh[1][j & 1] != 0;
-                keep_sh[1][(j + 1) & 1] = 0u;
-              }
-              if (keep1) {
-                if (!vload && !(ok = issue_v(j))) break;
-                vload = true;
+              {
                 ok = mbar_wait(&bar[B_PRDY + 1], pr1 & 1, limit, kSpinIssuer);
                 ++pr1;
                 if (!ok || !(ok = wait_v())) break;
@@ -597,18 +426,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
               mma_commit(&bar[B_KE + st]);
               ++kc;
             }
-            if (vload) {   // keep the V ring in step even if nobody used the tile
-              if (!(ok = wait_v())) break;
-              mma_commit(&bar[B_VE + vs]);
-              ++vc;
-            }
+            if (!(ok = wait_v())) break;
+            mma_commit(&bar[B_VE + vs]);
+            ++vc;
           }
         } while (false);
         ctr_sh[3] = qc;
         ctr_sh[4] = kc;
         ctr_sh[5] = vc;
-        ctr_sh[6] = vt0;
-        ctr_sh[7] = vt1;
         ctr_sh[8] = pr0;
         ctr_sh[9] = pr1;
       }
@@ -645,8 +470,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           const int doff = doff0 - j * kTile;   // row r sees columns <= r + doff
           const bool diag = p.causal && doff < kTile - 1;
           const bool tailt = tail && j == nk - 1;
-          if (v_prefetch && have_kept) {
-            // ---- skipping off, after the first tile: one pass over S. P is
+          if (have_kept) {
+            // ---- after the first tile: one pass over S. P is
             // computed against the current reference max while the row max is
             // taken; only when a row's max outgrows the reference by more than
             // 2^8 is O rescaled and the tile's P recomputed (S is still intact:
@@ -776,53 +601,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             rm = max3f(max3f(acc[0], acc[1], acc[2]), max3f(acc[3], acc[4], acc[5]),
                        fmaxf(acc[6], acc[7]));
           }
-          const float trm = rm * c;
-          const bool pred = !valid || (trm < m2 + p.log2_lambda);
-          tc_fence_before();
-          // each warp posts its vote as soon as it has it (the MMA warp acts on
-          // all four arrivals); the warpgroup's own decision is the barrier's
-          if (!v_prefetch) {   // with skipping off there is nothing to vote on
-            const bool wkeep = !__all_sync(0xffffffffu, pred);
-            if (lane == 0) {
-              if (wkeep) atomicOr(const_cast<uint32_t *>(&keep_sh[slot][j & 1]), 1u);
-              mbar_arrive(&bar[B_VOTE + slot]);
-            }
-          }
-          const bool skip = bar_red_and(pred, barid, 128);
-          if (abort_sh) {   // read after the barrier: uniform over the warpgroup
-            ok = false;
-            break;
-          }
-          if (skip) {
-            if (row == 0) word |= 1u << (j & 31);
-          } else {
-            const float mnew = valid ? fmaxf(m2, trm) : 0.f;
-            if (have_kept) {
-              // the previous P.V of this slot is complete by now (it was issued
-              // before this tile's S); waiting keeps the phase count exact and
-              // orders the O rescale after it
-              if (!mbar_wait(&bar[B_PV + slot], pvc & 1, limit)) abort_sh = 1;
-              ++pvc;
-              tc_fence_after();
-              const bool need = valid && (mnew - mref > kRescaleLog2);
-              if (__any_sync(0xffffffffu, need)) {
-                const float alpha = need ? ex2_approx(mref - mnew) : 1.f;
-                l *= alpha;
-                if (need) mref = mnew;
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                  uint32_t v[32];
-                  tmem_ld32(tO + ch * 32, v);
-                  tmem_wait_ld(v);
-#pragma unroll
-                  for (int e = 0; e < 32; ++e)
-                    v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                  tmem_st32(tO + ch * 32, v);
-                }
-              }
-            } else {
-              mref = mnew;
-            }
+          // ---- the first tile: the row max first, then P against it
+          {
+            const float mnew = valid ? rm * c : 0.f;
+            mref = mnew;
             m2 = mnew;
             // P = exp2(S c - m_ref), written over the S columns already read:
             // chunk ch (keys 32ch..32ch+31) goes to columns 16ch.. (bf16) or 8ch.. (e4m3)
@@ -963,28 +745,18 @@ size_t forward_smem_bytes() { return SM_BYTES + 1024; }
 
 cudaError_t launch_forward(const FwdParams &p, bool fp8, int num_ctas, cudaStream_t stream) {
   const size_t smem = forward_smem_bytes();
-  const bool skip = p.log2_lambda > -INFINITY;
-  if (fp8) {
-    if (skip)
-      fwd_kernel<true, true><<<num_ctas, kFwdThreads, smem, stream>>>(p);
-    else
-      fwd_kernel<true, false><<<num_ctas, kFwdThreads, smem, stream>>>(p);
-  } else {
-    if (skip)
-      fwd_kernel<false, true><<<num_ctas, kFwdThreads, smem, stream>>>(p);
-    else
-      fwd_kernel<false, false><<<num_ctas, kFwdThreads, smem, stream>>>(p);
-  }
+  if (fp8)
+    fwd_kernel<true><<<num_ctas, kFwdThreads, smem, stream>>>(p);
+  else
+    fwd_kernel<false><<<num_ctas, kFwdThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t prepare_forward() {
   const int smem = (int)forward_smem_bytes();
   const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<false, true>, a, smem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<false, false>, a, smem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<true, true>, a, smem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<true, false>, a, smem);
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<false>, a, smem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<true>, a, smem);
   return e;
 }
 

@@ -80,9 +80,14 @@ cudaError_t launch_prologue(const int32_t *cu_seqlens, const int32_t *cu_seqlens
                             int max_pages, int num_pages, Workspace *ws,
                             const WorkspaceLayout &layout, const CUtensorMap tmpl[3],
                             cudaStream_t stream);
+// Dense forward (lambda = 0): one online-softmax pass over every causal tile.
 cudaError_t launch_forward(const FwdParams &p, bool fp8, int num_ctas, cudaStream_t stream);
 size_t forward_smem_bytes();
 cudaError_t prepare_forward();   // per device: opt in to the shared-memory size
+// Skipping forward (lambda > 0, bsa_skip.cu): scan of every causal tile for the
+// decisions, then the kept tiles.
+cudaError_t launch_skip(const FwdParams &p, bool fp8, int num_ctas, cudaStream_t stream);
+cudaError_t prepare_skip();
 
 // FP8 scales registered on the calling thread (bsa_api.cu).
 void current_fp8_scales(const float **q, const float **k, const float **v);

@@ -66,7 +66,8 @@ bsa_status_t setup_device(int dev, DeviceSetup **out) {
     if (s.supported) {
       void *ptr = nullptr;
       if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return BSA_ERR_CUDA;
-      if (bsa::prepare_forward() != cudaSuccess) return BSA_ERR_CUDA;
+      if (bsa::prepare_forward() != cudaSuccess || bsa::prepare_skip() != cudaSuccess)
+        return BSA_ERR_CUDA;
       s.scratch = ptr;
     }
     if (!g_encode) {
@@ -167,6 +168,8 @@ extern "C" bsa_status_t bsa_prefill_fwd_noalloc(
   p.log2_lambda = lambda > 0.f ? (float)std::log2((double)lambda) : -INFINITY;
   p.wait_limit_ns = 2000000000ull;
   p.debug_drop_k_load = -1;
-  if (bsa::launch_forward(p, fp8, s->sm_count, stream) != cudaSuccess) return BSA_ERR_CUDA;
+  const cudaError_t e = lambda > 0.f ? bsa::launch_skip(p, fp8, s->sm_count, stream)
+                                     : bsa::launch_forward(p, fp8, s->sm_count, stream);
+  if (e != cudaSuccess) return BSA_ERR_CUDA;
   return BSA_OK;
 }

@@ -111,19 +111,6 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ bool bar_red_and(bool pred, uint32_t id, uint32_t count) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)pred), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
-}
-
 __device__ __forceinline__ bool bar_red_or(bool pred, uint32_t id, uint32_t count) {
   uint32_t r;
   asm volatile(
@@ -171,6 +158,18 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Per-warpgroup register budget (all four warps of a warpgroup execute it):
+// lower this warpgroup's registers per thread to N, or wait until the pool
+// given back by other warpgroups lets them rise to N.
+template <uint32_t N>
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
