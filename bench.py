@@ -208,6 +208,32 @@ def _oracle_item(args):
     return time.perf_counter() - t0
 
 
+def _c0_walk():
+    """The oracle on the whole small single-head layer (2048 tokens, every
+    query tile), pinned to one core (run in a child with one BLAS thread)."""
+    os.sched_setaffinity(0, {min(os.sched_getaffinity(0))})
+    from gen import inputs as gi
+    from oracle import numerics, tile_walk
+    p = gi.config("C0")
+    q, k, v = (numerics.bf16_to_f64(x) for x in (p.q, p.k, p.v))
+    t0 = time.perf_counter()
+    tile_walk.prefill_fwd(q, k, v, p.cu_seqlens, p.Hq, p.Hkv, lam=0.01)
+    ms = (time.perf_counter() - t0) * 1e3
+    return {"workload": "single head, 2048 tokens, d=128, causal, lambda=0.01 (all 16 query tiles)",
+            "ms": round(ms, 2), "dense_equiv_tflops": round(dense_flops([2048], 1) / (ms * 1e-3) / 1e12, 6),
+            "cores": 1}
+
+
+def oracle_c0_one_core():
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, "-c", "import bench, json; print(json.dumps(bench._c0_walk()))"],
+                           cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, not fatal
+        return {"error": str(e)[:200]}
+
+
 def chunk_dense_flops(lq, lk, Hq, d=128):
     """Dense causal FLOPs of lq queries at the last positions of lk keys."""
     off = lk - lq
@@ -282,6 +308,99 @@ def oracle_baseline(problem, budget_s: float = 12.0, cores=None, seed: int = 0, 
     return flops / wall / 1e12, cores, desc, wall, len(items)
 
 
+# ------------------------------------------------------------------ GPU helpers
+
+def kv_bytes(bits, seqlens, Hq, Hkv, d, elem=2):
+    """Algorithmic HBM bytes of the K/V stream for one launch: every K tile
+    once per KV head, and every V tile that at least one query tile of the
+    KV head's group keeps, once."""
+    G = Hq // Hkv
+    total, off = 0, 0
+    for L in seqlens:
+        n = (L + TILE - 1) // TILE
+        W = (n + 31) // 32
+        rows = np.ascontiguousarray(bits[off:off + Hq * n * W]).view(np.uint32).reshape(Hq, n, W)
+        off += Hq * n * W
+        skip = np.unpackbits(rows.view(np.uint8), axis=2, bitorder="little")[:, :, :n].astype(bool)
+        visited = np.tril(np.ones((n, n), bool))
+        kept = (~skip) & visited[None]
+        v_tiles = int(kept.reshape(Hkv, G * n, n).any(axis=1).sum())
+        tok_bytes = TILE * d * elem
+        total += Hkv * n * tok_bytes + v_tiles * tok_bytes
+    return int(total)
+
+
+def fp8_peak(dev, n=8192, reps=10):
+    """Dense E4M3 GEMM rate of the box's library (torch._scaled_mm, n^3,
+    bf16 output, best of ``reps``), with and without fast accumulation."""
+    import torch
+    out = {"how": f"torch._scaled_mm e4m3 {n}^3 -> bf16, best of {reps} (CUDA events)"}
+    try:
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        one = torch.tensor(1.0, device=dev)
+        for fast in (False, True):
+            def mm():
+                return torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16,
+                                        use_fast_accum=fast)
+            for _ in range(3):
+                mm()
+            best = float("inf")
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                mm()
+                e1.record()
+                torch.cuda.synchronize()
+                best = min(best, e0.elapsed_time(e1))
+            out["fast_accum" if fast else "tflops"] = round(2.0 * n ** 3 / (best * 1e-3) / 1e12, 1)
+        out["peak"] = max(out["tflops"], out["fast_accum"])
+        del a, b
+    except Exception as e:  # a missing FP8 GEMM is reported, not fatal
+        out["error"] = str(e)[:200]
+    return out
+
+
+def sdpa_backends(q, k, v, T, Hq, Hkv, d, dflops, peak, steps, stream):
+    """torch SDPA (dense causal) on the same shape with each backend forced;
+    K/V heads expanded to Hq outside the timed region. Returns the fastest
+    backend's line and every backend's time or error."""
+    import torch
+    import torch.nn.functional as F
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+    Q = q.view(1, T, Hq, d).transpose(1, 2)
+    K = k.view(1, T, Hkv, d).transpose(1, 2).repeat_interleave(Hq // Hkv, dim=1)
+    V = v.view(1, T, Hkv, d).transpose(1, 2).repeat_interleave(Hq // Hkv, dim=1)
+    results = {}
+    for name, be in (("cudnn", SDPBackend.CUDNN_ATTENTION), ("flash", SDPBackend.FLASH_ATTENTION),
+                     ("efficient", SDPBackend.EFFICIENT_ATTENTION)):
+        try:
+            with sdpa_kernel([be]):
+                o = F.scaled_dot_product_attention(Q, K, V, is_causal=True)
+                torch.cuda.synchronize()
+                n = max(2, steps // 4)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(n):
+                    o = F.scaled_dot_product_attention(Q, K, V, is_causal=True)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                results[name] = round(e0.elapsed_time(e1) / n, 3)
+                del o
+        except Exception as e:
+            results[name] = "unavailable: " + str(e).splitlines()[0][:160]
+    del K, V
+    timed_ok = {k_: v_ for k_, v_ in results.items() if isinstance(v_, float)}
+    if not timed_ok:
+        return {"impl": "torch SDPA", "error": "no backend ran", "backends_ms": results}
+    best = min(timed_ok, key=timed_ok.get)
+    m = timed_ok[best]
+    return {"impl": f"torch.nn.functional.scaled_dot_product_attention, {best} backend (is_causal, "
+                    f"K/V heads expanded)", "backend": best, "ms": m,
+            "dense_tflops": round(dflops / m / 1e9, 1), "frac_of_peak": round(dflops / m / 1e9 / peak, 4),
+            "backends_ms": results}
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def gpu_arm(args, rank, world, local_rank):
@@ -318,25 +437,29 @@ def gpu_arm(args, rank, world, local_rank):
             raise bsa.BsaError(st, "bsa_prefill_fwd")
 
     def timed(nsteps, lam=args.lam):
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        """(median, mean) ms per step over nsteps steps: an event before every
+        step and one after the last, all on the launching stream."""
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(nsteps + 1)]
         barrier(world)
         torch.cuda.synchronize()
-        ev0.record(stream)
-        for _ in range(nsteps):
+        for i in range(nsteps):
+            evs[i].record(stream)
             step(lam)
-        ev1.record(stream)
+        evs[nsteps].record(stream)
         torch.cuda.synchronize()
         barrier(world)
-        return ev0.elapsed_time(ev1) / nsteps
+        per = [evs[i].elapsed_time(evs[i + 1]) for i in range(nsteps)]
+        return statistics.median(per), evs[0].elapsed_time(evs[nsteps]) / nsteps
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     bsa.check(bsa.get_device_status(stream), "device status")
     with ClockSampler(local_rank) as clk:
-        ms = timed(args.steps)
+        ms, ms_mean = timed(args.steps)
     clocks = clk.summary()
     ms = max_over_ranks(ms, world, dev)
+    ms_mean = max_over_ranks(ms_mean, world, dev)
     bsa.check(bsa.get_device_status(stream), "device status")
     skipped = popcount(bm.cpu().numpy())
     ctiles = causal_tiles(seqlens, Hq)
@@ -352,13 +475,24 @@ def gpu_arm(args, rank, world, local_rank):
     peak = peaks.get("bf16_tflops", 1900.0)
     achieved = xflops / (ms * 1e-3) / 1e12
     traffic = measured_traffic() if args.config == "C2" else None
+    kv = kv_bytes(bm.cpu().numpy(), seqlens, Hq, Hkv, d)
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "algorithmic_bytes": int(2 * (p.q.size + p.k.size + p.v.size + p.q.size) + 4 * Hq * T),
-                "peak_source": "MEASURED_PEAKS.json bf16_tflops (burst)" if "bf16_tflops" in peaks
-                else "fallback 1900 TFLOP/s", "flops_per_launch": xflops}
-    if "bf16_tflops_sustained" in peaks:   # the same work against the seconds-long cuBLAS rate
-        roofline["frac_of_sustained"] = round(achieved / peaks["bf16_tflops_sustained"], 4)
+                "peak_source": "MEASURED_PEAKS.json bf16_tflops (burst), of measured"
+                if "bf16_tflops" in peaks else "fallback 1900 TFLOP/s, of fallback",
+                "flops_per_launch": xflops,
+                "kv_hbm": {"bytes": kv, "gbs": round(kv / (ms * 1e-3) / 1e9, 2),
+                           "what": "K once per KV head + V of every key tile some query tile keeps, "
+                                   "once (the K/V stream's algorithmic HBM bytes)"}}
+    if "bf16_tflops_sustained" in peaks and clocks and clocks.get("sm_mhz"):
+        # secondary: the seconds-long cuBLAS rate, both normalised by their median SM clock
+        pk = peaks.get("clocks_under_load", {}).get("sm_mhz_median")
+        if pk:
+            roofline["secondary_sustained"] = {
+                "peak": peaks["bf16_tflops_sustained"], "peak_sm_mhz": pk, "run_sm_mhz": clocks["sm_mhz"],
+                "frac_per_clock": round((achieved / clocks["sm_mhz"]) /
+                                        (peaks["bf16_tflops_sustained"] / pk), 4)}
 
     # lambda sweep on the same layer (skip fraction and TFLOP/s for each lambda)
     sweep = []
@@ -366,17 +500,17 @@ def gpu_arm(args, rank, world, local_rank):
         for lam in (0.0, 1e-3, 1e-2, 5e-2):
             step(lam)
             torch.cuda.synchronize()
-            m = timed(max(2, args.steps // 2), lam)
+            m, _ = timed(max(2, args.steps // 2), lam)
             sk = popcount(bm.cpu().numpy())
             sweep.append({"lambda": lam, "ms": round(m, 3), "dense_equiv_tflops": round(dflops / m / 1e9, 1),
                           "executed_tflops": round(executed_flops(seqlens, Hq, sk, d) / m / 1e9, 1),
                           "skip_fraction": round(sk / ctiles, 5)})
 
     # FP8 E4M3 variant of the same layer (C4): per-head quantisation by the
-    # library, then the FP8 forward; its tensor peak is the measured bf16
-    # peak times the nominal FP8/bf16 ratio of 2
+    # library, then the FP8 forward, against the box's measured E4M3 GEMM rate
     fp8 = None
     if not args.no_fp8:
+        f8peak = fp8_peak(dev)
         codes = [torch.empty(x.shape, dtype=torch.uint8, device=dev) for x in (q, k, v)]
         scales = [torch.empty((x.shape[1],), dtype=torch.float32, device=dev) for x in (q, k, v)]
         for x, c8, sc in zip((q, k, v), codes, scales):
@@ -401,11 +535,16 @@ def gpu_arm(args, rank, world, local_rank):
         m8 = ev0.elapsed_time(ev1) / n8
         sk8 = popcount(bm.cpu().numpy())
         x8 = executed_flops(seqlens, Hq, sk8, d)
+        if "peak" in f8peak:
+            p8, p8src = f8peak["peak"], "measured in this run: " + f8peak["how"]
+        else:
+            p8, p8src = 2 * peak, "measured bf16 burst x nominal FP8/bf16 ratio 2 (FP8 GEMM unavailable)"
         fp8 = {"workload": "the same layer in FP8 E4M3 (per-head absmax scales), bf16 output",
                "lambda": args.lam, "ms": round(m8, 3), "dense_equiv_tflops": round(dflops / m8 / 1e9, 1),
                "executed_tflops": round(x8 / m8 / 1e9, 1), "skip_fraction": round(sk8 / ctiles, 5),
-               "roofline_frac": round(x8 / m8 / 1e9 / (2 * peak), 4),
-               "peak": 2 * peak, "peak_source": "measured bf16 burst x nominal FP8/bf16 ratio 2"}
+               "roofline_frac": round(x8 / m8 / 1e9 / p8, 4), "peak": p8, "peak_source": p8src,
+               "fp8_gemm": f8peak,
+               "kv_hbm_gbs": round(kv_bytes(bm.cpu().numpy(), seqlens, Hq, Hkv, d, 1) / (m8 * 1e-3) / 1e9, 2)}
         bsa.check(bsa.set_fp8_scales(None, None, None), "clear scales")
         bsa.check(bsa.get_device_status(stream), "device status")
         del codes, scales
@@ -571,35 +710,12 @@ def gpu_arm(args, rank, world, local_rank):
                 "executed_tflops": round(xd / md / 1e9, 1), "roofline_frac": round(xd / md / 1e9 / peak, 4)}
         del qd, kd, vd, outd, lsed, bmd
 
-    # dense causal attention from the box's library (torch SDPA) on the same
-    # shape: the comparison for the lambda = 0 path
+    # dense causal attention from the box's library (torch SDPA, every
+    # backend forced in turn) on the same shape: the comparison for the
+    # lambda = 0 path
     dense_ref = None
     if not args.no_sweep and p.n_seqs == 1:
-        try:
-            import torch.nn.functional as F
-            Q = q.view(1, T, Hq, d).transpose(1, 2)
-            K = k.view(1, T, Hkv, d).transpose(1, 2)
-            V = v.view(1, T, Hkv, d).transpose(1, 2)
-
-            def sdpa():
-                return F.scaled_dot_product_attention(Q, K, V, is_causal=True, enable_gqa=True)
-            for _ in range(2):
-                o_ref = sdpa()
-            torch.cuda.synchronize()
-            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            n_ref = max(2, args.steps // 2)
-            ev0.record(stream)
-            for _ in range(n_ref):
-                o_ref = sdpa()
-            ev1.record(stream)
-            torch.cuda.synchronize()
-            m = ev0.elapsed_time(ev1) / n_ref
-            dense_ref = {"impl": "torch.nn.functional.scaled_dot_product_attention (is_causal, GQA)",
-                         "ms": round(m, 3), "dense_tflops": round(dflops / m / 1e9, 1),
-                         "frac_of_peak": round(dflops / m / 1e9 / peak, 4)}
-            del o_ref
-        except Exception as e:  # a missing backend is reported, not fatal
-            dense_ref = {"impl": "torch SDPA", "error": str(e)[:200]}
+        dense_ref = sdpa_backends(q, k, v, T, Hq, Hkv, d, dflops, peak, args.steps, stream)
 
     # end to end through the C interface with host buffers: every step copies
     # its inputs in from pinned host memory and its results (out, lse, skip
@@ -686,11 +802,14 @@ def gpu_arm(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, cores, desc, wall, nitems = oracle_baseline(p, budget_s=args.cpu_budget)
         cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
-               "wall_s": round(wall, 2)}
+               "wall_s": round(wall, 2), "extrapolated": True,
+               "extrapolation": "throughput of the sampled query tiles stands for the whole layer",
+               "c0_1core": oracle_c0_one_core()}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "ms_per_step_mean": round(ms_mean, 3), "timing": "median of per-step CUDA-event times",
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded generator: sink + local-window bias, Llama-3-8B attention shape)",
         "config": {"workload": WORKLOADS.get(args.config, args.config), "name": args.config,

@@ -66,6 +66,10 @@ def lib() -> ctypes.CDLL:
     L.bsa_version.restype = i32
     L.bsa_release.argtypes = []
     L.bsa_release.restype = None
+    L.bsa_release_stream.argtypes = [vp]
+    L.bsa_release_stream.restype = i32
+    L.bsa_get_noalloc_status.argtypes = [vp]
+    L.bsa_get_noalloc_status.restype = i32
     L.bsa_debug_fault_drill.argtypes = [i32, i64]
     L.bsa_debug_fault_drill.restype = i32
     L.bsa_decode_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32, i32, f32, vp,
@@ -197,6 +201,16 @@ def importance_blocks(cu_seqlens_host) -> int:
 
 def get_device_status(stream=None) -> int:
     return lib().bsa_get_device_status(_stream(stream))
+
+
+def get_noalloc_status(stream=None) -> int:
+    """bsa_get_noalloc_status: device-side status of the no-allocation calls."""
+    return lib().bsa_get_noalloc_status(_stream(stream))
+
+
+def release_stream(stream=None) -> int:
+    """bsa_release_stream: free the scratch kept for one stream."""
+    return lib().bsa_release_stream(_stream(stream))
 
 
 def status_string(status: int) -> str:

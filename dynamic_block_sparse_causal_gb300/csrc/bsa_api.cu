@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstring>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <utility>
 
@@ -21,26 +22,30 @@ namespace {
 using bsa::Workspace;
 using bsa::WorkspaceLayout;
 
-struct StreamScratch {
-  Workspace *ws = nullptr;
-  size_t bytes = 0;
-};
-
 struct DeviceInfo {
   bool ready = false;
   bool supported = false;
   int sm_count = 0;
 };
 
-std::mutex g_mu;
-std::map<std::pair<int, cudaStream_t>, StreamScratch> g_scratch;
-// block-importance tables per (device, stream), grown like the scratch area
-struct ImpScratch {
+// A growable device buffer, grown stream-ordered.
+struct Buffer {
   void *ptr = nullptr;
   size_t bytes = 0;
 };
-std::map<std::pair<int, cudaStream_t>, ImpScratch> g_imp_scratch;
-std::map<std::pair<int, cudaStream_t>, ImpScratch> g_dec_scratch;   // decode tables
+
+// Everything the library keeps for one (device, stream): the scratch area of
+// the prefill and top-p calls (work queue, tensor maps, status word, tables),
+// the block-importance tables and the decode tables. Calls on one stream
+// share it, so `mu` serialises them from enqueue to the last launch; calls on
+// different streams only meet briefly on g_mu, for the lookup.
+struct StreamState {
+  std::mutex mu;
+  Buffer ws, imp, dec;
+};
+
+std::mutex g_mu;   // guards g_streams, g_devices and g_encode
+std::map<std::pair<int, cudaStream_t>, std::unique_ptr<StreamState>> g_streams;
 std::map<int, DeviceInfo> g_devices;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -52,7 +57,7 @@ thread_local uint64_t t_wait_limit_ns = 2000000000ull;  // 2 s
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Resolve the driver's tensor-map encoder once (no link-time libcuda).
+// Resolve the driver's tensor-map encoder once (no link-time libcuda). Under g_mu.
 bool encoder() {
   if (g_encode) return true;
   void *fn = nullptr;
@@ -65,7 +70,11 @@ bool encoder() {
   return true;
 }
 
+// Per-device set-up (capability, SM count, kernel attributes) and the
+// tensor-map encoder, once; the returned record is not modified afterwards.
 bsa_status_t device_info(int dev, DeviceInfo **out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!encoder()) return BSA_ERR_CUDA;
   DeviceInfo &d = g_devices[dev];
   if (!d.ready) {
     int major = 0, minor = 0;
@@ -84,30 +93,37 @@ bsa_status_t device_info(int dev, DeviceInfo **out) {
   return BSA_OK;
 }
 
-// Scratch area of (device, stream), grown stream-ordered when n_seqs grows.
-bsa_status_t scratch_for(int dev, cudaStream_t stream, size_t bytes, Workspace **out) {
-  StreamScratch &s = g_scratch[{dev, stream}];
+// The state of (device, stream), created on first use. The caller locks its mu.
+StreamState *stream_state(int dev, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  std::unique_ptr<StreamState> &p = g_streams[{dev, stream}];
+  if (!p) p.reset(new StreamState);
+  return p.get();
+}
+
+// Scratch area of a stream, grown stream-ordered when n_seqs grows. Under ss->mu.
+bsa_status_t scratch_for(StreamState *ss, cudaStream_t stream, size_t bytes, Workspace **out) {
+  Buffer &s = ss->ws;
   if (s.bytes < bytes) {
     void *p = nullptr;
     if (cudaMallocAsync(&p, bytes, stream) != cudaSuccess) return BSA_ERR_NO_MEMORY;
     if (cudaMemsetAsync(p, 0, sizeof(Workspace), stream) != cudaSuccess) return BSA_ERR_CUDA;
-    if (s.ws) {  // keep the sticky status word
-      if (cudaMemcpyAsync(&static_cast<Workspace *>(p)->status, &s.ws->status, sizeof(int32_t),
+    if (s.ptr) {  // keep the sticky status word
+      if (cudaMemcpyAsync(&static_cast<Workspace *>(p)->status,
+                          &static_cast<Workspace *>(s.ptr)->status, sizeof(int32_t),
                           cudaMemcpyDeviceToDevice, stream) != cudaSuccess ||
-          cudaFreeAsync(s.ws, stream) != cudaSuccess)
+          cudaFreeAsync(s.ptr, stream) != cudaSuccess)
         return BSA_ERR_CUDA;
     }
-    s.ws = static_cast<Workspace *>(p);
+    s.ptr = p;
     s.bytes = bytes;
   }
-  *out = s.ws;
+  *out = static_cast<Workspace *>(s.ptr);
   return BSA_OK;
 }
 
-// Block-importance or decode tables of (device, stream), grown stream-ordered.
-bsa_status_t imp_scratch_for(int dev, cudaStream_t stream, size_t bytes, void **out,
-                             std::map<std::pair<int, cudaStream_t>, ImpScratch> &pool = g_imp_scratch) {
-  ImpScratch &s = pool[{dev, stream}];
+// Block-importance or decode tables of a stream, grown stream-ordered. Under ss->mu.
+bsa_status_t table_for(Buffer &s, cudaStream_t stream, size_t bytes, void **out) {
   if (s.bytes < bytes) {
     void *p = nullptr;
     if (cudaMallocAsync(&p, bytes, stream) != cudaSuccess) return BSA_ERR_NO_MEMORY;
@@ -174,12 +190,10 @@ bsa_status_t prefill(const void *q, const void *k, const void *v, const int32_t 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
   DeviceInfo *info = nullptr;
   bsa_status_t st = device_info(dev, &info);
   if (st != BSA_OK) return st;
   if (!info->supported) return BSA_ERR_UNSUPPORTED;
-  if (!encoder()) return BSA_ERR_CUDA;
 
   CUtensorMap tmpl[3];
   const uint64_t kv_tokens = page_table ? (uint64_t)num_pages * bsa::kTile : 1;
@@ -188,8 +202,10 @@ bsa_status_t prefill(const void *q, const void *k, const void *v, const int32_t 
     return BSA_ERR_INVALID_ARG;
 
   const WorkspaceLayout layout = WorkspaceLayout::make(n_seqs);
+  StreamState *ss = stream_state(dev, stream);
+  std::lock_guard<std::mutex> lock(ss->mu);
   Workspace *ws = nullptr;
-  if ((st = scratch_for(dev, stream, layout.bytes, &ws)) != BSA_OK) return st;
+  if ((st = scratch_for(ss, stream, layout.bytes, &ws)) != BSA_OK) return st;
   if (bsa::launch_prologue(cu_seqlens, cu_seqlens_k, n_seqs, Hq, Hkv, causal, page_table,
                            max_pages, num_pages, ws, layout, tmpl, stream) != cudaSuccess)
     return BSA_ERR_CUDA;
@@ -287,24 +303,24 @@ bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
   DeviceInfo *info = nullptr;
   bsa_status_t st = device_info(dev, &info);
   if (st != BSA_OK) return st;
   if (!info->supported) return BSA_ERR_UNSUPPORTED;
-  if (!encoder()) return BSA_ERR_CUDA;
   CUtensorMap tk, tv;
   const uint64_t extent = total_k > 0 ? (uint64_t)total_k : 1;
   if (!encode_tile_map(&tk, k, Hkv, false, extent) || !encode_tile_map(&tv, v, Hkv, false, extent))
     return BSA_ERR_INVALID_ARG;
+  StreamState *ss = stream_state(dev, stream);
+  std::lock_guard<std::mutex> lock(ss->mu);
   Workspace *ws = nullptr;
-  if ((st = scratch_for(dev, stream, sizeof(Workspace), &ws)) != BSA_OK) return st;
+  if ((st = scratch_for(ss, stream, sizeof(Workspace), &ws)) != BSA_OK) return st;
   const int rows = group * max_seqlen_q;
   // 16-tile splits unless that leaves fewer than four work items per SM
   const int split = (int64_t)Hkv * (total_k / bsa::kTile) / 16 < 4LL * info->sm_count ? 8 : 16;
   const bsa::DecLayout layout = bsa::DecLayout::make(n_seqs, Hq, Hkv, rows, total_k, split);
   void *buf = nullptr;
-  if ((st = imp_scratch_for(dev, stream, layout.bytes, &buf, g_dec_scratch)) != BSA_OK) return st;
+  if ((st = table_for(ss->dec, stream, layout.bytes, &buf)) != BSA_OK) return st;
   char *base = static_cast<char *>(buf);
   bsa::DecParams p{};
   p.dw = static_cast<bsa::DecWorkspace *>(buf);
@@ -373,12 +389,10 @@ bsa_status_t bsa_block_importance(const void *q, const void *k, const int32_t *c
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
   DeviceInfo *info = nullptr;
   bsa_status_t st = device_info(dev, &info);
   if (st != BSA_OK) return st;
   if (!info->supported) return BSA_ERR_UNSUPPORTED;
-  if (!encoder()) return BSA_ERR_CUDA;
 
   CUtensorMap tmpl[2];
   // Q in 64-row boxes: a tile is one head's last 128 positions or the last
@@ -386,11 +400,13 @@ bsa_status_t bsa_block_importance(const void *q, const void *k, const int32_t *c
   if (!encode_tile_map(&tmpl[0], q, Hq, false, 1, bsa::kTile / 2) ||
       !encode_tile_map(&tmpl[1], k, Hkv, false))
     return BSA_ERR_INVALID_ARG;
+  StreamState *ss = stream_state(dev, stream);
+  std::lock_guard<std::mutex> lock(ss->mu);
   Workspace *ws = nullptr;   // holds the status word
-  if ((st = scratch_for(dev, stream, sizeof(Workspace), &ws)) != BSA_OK) return st;
+  if ((st = scratch_for(ss, stream, sizeof(Workspace), &ws)) != BSA_OK) return st;
   const bsa::ImpLayout layout = bsa::ImpLayout::make(n_seqs, Hq, total_blocks);
   void *buf = nullptr;
-  if ((st = imp_scratch_for(dev, stream, layout.bytes, &buf)) != BSA_OK) return st;
+  if ((st = table_for(ss->imp, stream, layout.bytes, &buf)) != BSA_OK) return st;
   char *base = static_cast<char *>(buf);
 
   bsa::ImpParams p{};
@@ -434,13 +450,14 @@ bsa_status_t bsa_top_p_select(const float *scores, const int32_t *cu_seqlens, in
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
   DeviceInfo *info = nullptr;
   bsa_status_t st = device_info(dev, &info);
   if (st != BSA_OK) return st;
   if (!info->supported) return BSA_ERR_UNSUPPORTED;
+  StreamState *ss = stream_state(dev, stream);
+  std::lock_guard<std::mutex> lock(ss->mu);
   Workspace *ws = nullptr;
-  if ((st = scratch_for(dev, stream, sizeof(Workspace), &ws)) != BSA_OK) return st;
+  if ((st = scratch_for(ss, stream, sizeof(Workspace), &ws)) != BSA_OK) return st;
   if (bsa::launch_top_p(scores, cu_seqlens, n_seqs, total_blocks, p, order, n_selected, keep, ws,
                         stream) != cudaSuccess)
     return BSA_ERR_CUDA;
@@ -500,13 +517,19 @@ bsa_status_t bsa_get_device_status(bsa_stream_t stream_) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return BSA_ERR_CUDA;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
-  auto it = g_scratch.find({dev, stream});
-  if (it == g_scratch.end() || !it->second.ws) return BSA_OK;
+  StreamState *ss = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_streams.find({dev, stream});
+    if (it == g_streams.end()) return BSA_OK;
+    ss = it->second.get();
+  }
+  std::lock_guard<std::mutex> lock(ss->mu);
+  if (!ss->ws.ptr) return BSA_OK;
+  int32_t *word = &static_cast<Workspace *>(ss->ws.ptr)->status;
   int32_t status = 0;
-  if (cudaMemcpy(&status, &it->second.ws->status, sizeof(status), cudaMemcpyDeviceToHost) !=
-          cudaSuccess ||
-      cudaMemset(&it->second.ws->status, 0, sizeof(status)) != cudaSuccess)
+  if (cudaMemcpy(&status, word, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(word, 0, sizeof(status)) != cudaSuccess)
     return BSA_ERR_CUDA;
   if (status & bsa::kStatusBadSeqlens) return BSA_ERR_BAD_SEQLENS;
   if (status & bsa::kStatusTimeout) return BSA_ERR_TIMEOUT;
@@ -526,34 +549,39 @@ const char *bsa_status_string(bsa_status_t s) {
   return "unknown status";
 }
 
-int32_t bsa_version(void) { return 100; }
+int32_t bsa_version(void) { return 200; }
 
 void bsa_release(void) {
   std::lock_guard<std::mutex> lock(g_mu);
   int cur = 0;
   cudaGetDevice(&cur);
-  for (auto &kv : g_scratch) {
-    if (kv.second.ws) {
-      cudaSetDevice(kv.first.first);
-      cudaFree(kv.second.ws);
-    }
+  for (auto &kv : g_streams) {
+    std::lock_guard<std::mutex> slock(kv.second->mu);
+    cudaSetDevice(kv.first.first);
+    for (Buffer *b : {&kv.second->ws, &kv.second->imp, &kv.second->dec})
+      if (b->ptr) cudaFree(b->ptr);
   }
-  g_scratch.clear();
-  for (auto &kv : g_imp_scratch) {
-    if (kv.second.ptr) {
-      cudaSetDevice(kv.first.first);
-      cudaFree(kv.second.ptr);
-    }
-  }
-  g_imp_scratch.clear();
-  for (auto &kv : g_dec_scratch) {
-    if (kv.second.ptr) {
-      cudaSetDevice(kv.first.first);
-      cudaFree(kv.second.ptr);
-    }
-  }
-  g_dec_scratch.clear();
+  g_streams.clear();
   cudaSetDevice(cur);
+}
+
+bsa_status_t bsa_release_stream(bsa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+  std::unique_ptr<StreamState> ss;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_streams.find({dev, stream});
+    if (it == g_streams.end()) return BSA_OK;
+    ss = std::move(it->second);
+    g_streams.erase(it);
+  }
+  std::lock_guard<std::mutex> slock(ss->mu);   // a call still enqueueing on it finishes first
+  bsa_status_t st = BSA_OK;
+  for (Buffer *b : {&ss->ws, &ss->imp, &ss->dec})
+    if (b->ptr && cudaFreeAsync(b->ptr, stream) != cudaSuccess) st = BSA_ERR_CUDA;
+  return st;
 }
 
 bsa_status_t bsa_debug_fault_drill(int32_t drop_k_load, int64_t wait_limit_ns) {

@@ -11,10 +11,12 @@
 //
 // The scratch array (kNoAllocScratchBytes, about 270 KiB) lives in device
 // global memory of every GPU that loads the library, for the life of the
-// process. Its address is looked up once per device with
-// cudaGetSymbolAddress, by the first call made on that device. Every call
-// shares the array, so calls whose work overlaps on the GPU (for example on
-// two streams at once) race on it; calls on one stream are ordered.
+// process. Its address is looked up with cudaGetSymbolAddress by the first
+// call made in each device context (a new context after cudaDeviceReset
+// gets its own look-up). Every call shares the array, so calls whose work
+// overlaps on the GPU (for example on two streams at once) race on it;
+// calls on one stream are ordered. Device-side errors accumulate in the
+// array's status word until bsa_get_noalloc_status() reads and clears it.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -42,20 +44,39 @@ struct DeviceSetup {
   bool done = false;
   bool supported = false;
   int sm_count = 0;
-  void *scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  CUcontext ctx = nullptr;  // the context the address below belongs to
+  void *scratch = nullptr;  // device address of g_noalloc_scratch in that context
 };
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DeviceSetup g_setup[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
 
-// One-time set-up for the current device: its address of the scratch
-// array, its SM count, and the forward kernel's shared-memory opt-in.
+template <typename F>
+bool driver_entry(const char *name, int version, F *fn) {
+  void *p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !p)
+    return false;
+  *fn = reinterpret_cast<F>(p);
+  return true;
+}
+
+// Set-up for the current device and its current context, once per context:
+// the context's address of the scratch array, the SM count and the forward
+// kernels' shared-memory opt-in. Under g_mu.
 bsa_status_t setup_device(int dev, DeviceSetup **out) {
   if (dev < 0 || dev >= kMaxDevices) return BSA_ERR_UNSUPPORTED;
   if (kLayout.bytes > kNoAllocScratchBytes) return BSA_ERR_UNSUPPORTED;
+  if (!g_ctx_current && !driver_entry("cuCtxGetCurrent", 4000, &g_ctx_current)) return BSA_ERR_CUDA;
+  // null before the runtime has made a context current on this thread
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return BSA_ERR_CUDA;
   DeviceSetup &s = g_setup[dev];
+  if (s.done && (!ctx || s.ctx != ctx)) s = DeviceSetup{};   // a new context (e.g. after a reset)
   if (!s.done) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -68,17 +89,12 @@ bsa_status_t setup_device(int dev, DeviceSetup **out) {
       if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return BSA_ERR_CUDA;
       if (bsa::prepare_forward() != cudaSuccess || bsa::prepare_skip() != cudaSuccess)
         return BSA_ERR_CUDA;
+      // the symbol look-up made the device's primary context current
+      if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return BSA_ERR_CUDA;
       s.scratch = ptr;
     }
-    if (!g_encode) {
-      void *fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                           cudaEnableDefault, &q) != cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || !fn)
-        return BSA_ERR_CUDA;
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
+    if (!g_encode && !driver_entry("cuTensorMapEncodeTiled", 12000, &g_encode)) return BSA_ERR_CUDA;
+    s.ctx = ctx;
     s.done = true;
   }
   *out = &s;
@@ -137,9 +153,9 @@ extern "C" bsa_status_t bsa_prefill_fwd_noalloc(
       !encode(&tmpl[2], v, Hkv, fp8))
     return BSA_ERR_INVALID_ARG;
 
+  // the status word keeps its bits until bsa_get_noalloc_status reads them;
+  // everything else the prologue rewrites
   bsa::Workspace *ws = static_cast<bsa::Workspace *>(s->scratch);
-  // The status word keeps the last call's bits: start this call from zero.
-  if (cudaMemsetAsync(&ws->status, 0, sizeof(int32_t), stream) != cudaSuccess) return BSA_ERR_CUDA;
   if (bsa::launch_prologue(cu_seqlens, cu_seqlens, n_seqs, Hq, Hkv, causal, nullptr, 0, 0, ws, kLayout, tmpl, stream) != cudaSuccess)
     return BSA_ERR_CUDA;
 
@@ -171,5 +187,25 @@ extern "C" bsa_status_t bsa_prefill_fwd_noalloc(
   const cudaError_t e = lambda > 0.f ? bsa::launch_skip(p, fp8, s->sm_count, stream)
                                      : bsa::launch_forward(p, fp8, s->sm_count, stream);
   if (e != cudaSuccess) return BSA_ERR_CUDA;
+  return BSA_OK;
+}
+
+extern "C" bsa_status_t bsa_get_noalloc_status(bsa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return BSA_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (dev < 0 || dev >= kMaxDevices || !g_setup[dev].done || !g_setup[dev].scratch) return BSA_OK;
+  CUcontext ctx = nullptr;
+  if (!g_ctx_current || g_ctx_current(&ctx) != CUDA_SUCCESS) return BSA_ERR_CUDA;
+  if (ctx != g_setup[dev].ctx) return BSA_OK;   // no call in this context yet
+  int32_t *word = &static_cast<bsa::Workspace *>(g_setup[dev].scratch)->status;
+  int32_t status = 0;
+  if (cudaMemcpy(&status, word, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(word, 0, sizeof(status)) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  if (status & bsa::kStatusBadSeqlens) return BSA_ERR_BAD_SEQLENS;
+  if (status & bsa::kStatusTimeout) return BSA_ERR_TIMEOUT;
   return BSA_OK;
 }

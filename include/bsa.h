@@ -31,8 +31,19 @@
  *    return BSA_ERR_CUDA. Errors found on the device (malformed cu_seqlens, a
  *    pipeline wait that ran out) are recorded in a per-stream status word
  *    that bsa_get_device_status() reads.
- *  - Calls on distinct streams may run concurrently; each stream has its own
- *    library-owned scratch area (work queue, tensor maps), grown on demand.
+ *  - Calls on distinct streams may run concurrently, from any host threads:
+ *    each (device, stream) has its own library-owned scratch area (work
+ *    queue, tensor maps, status word, tables), grown on demand and kept until
+ *    bsa_release_stream() or bsa_release(); host threads meet only briefly on
+ *    the lookup of that state. Calls on one stream from several host threads
+ *    are serialised by the library (they share its scratch area).
+ *  - Per call the one-CTA prologue ranks the sequences longest first in
+ *    O(n_seqs^2 / 1024) steps per thread and fills the level table in
+ *    O(n_seqs * max_tiles / 1024): about a microsecond at 16 sequences, a
+ *    few milliseconds at 10^5.
+ *  - Every sequence may have at most 65536 query tiles and 65536 key tiles
+ *    (8,388,608 tokens); longer ones are rejected on the device
+ *    (BSA_ERR_BAD_SEQLENS, nothing written).
  */
 #ifndef BSA_H
 #define BSA_H
@@ -80,7 +91,11 @@ typedef enum {
  * causal       1: causal (key position <= query position); 0: every key of
  *              the sequence is visible (same skip rule, all tiles visited).
  * lambda       skip threshold, 0 <= lambda < 1; 0 disables skipping. NaN
- *              is rejected.
+ *              is rejected. With lambda > 0 the decisions are taken first
+ *              for every causal key tile (QK^T and the row maxima only; a
+ *              skipped tile never raises the running max, so each decision
+ *              follows from the maxima of the tiles before it) and then the
+ *              kept tiles are computed; lambda = 0 runs one dense pass.
  * dtype        BSA_BF16, or BSA_FP8_E4M3 with scales set by
  *              bsa_set_fp8_scales() on the calling thread.
  * out          device bfloat16 [total_tokens, Hq, d]; must not overlap the
@@ -174,17 +189,18 @@ bsa_status_t bsa_prefill_fwd_paged(const void *q, const void *k_cache,
  * this is an interface variant, not part of the method.
  *
  * Allocates nothing: its scratch (work queue, tensor maps, scheduling
- * tables) is a fixed array of about 270 KiB compiled into the library and
- * resident on every GPU that loads it until the process exits. Limit:
- * n_seqs <= 1024 (larger batches return BSA_ERR_INVALID_ARG); sequences
- * longer than 8M tokens are rejected on the device as with bsa_prefill_fwd.
- * The first call on a device looks up that device's address of the array
- * (and sets the kernel's shared-memory limit); make that first call before
- * any stream capture. All calls share the one array and each call rewrites
- * it: calls whose GPU work overlaps (on different streams) race and must
- * not be issued; calls on one stream are safe. Device-side errors are not
- * reported by bsa_get_device_status; a malformed cu_seqlens leaves the
- * outputs unwritten.
+ * tables, status word) is a fixed array of about 270 KiB compiled into the
+ * library and resident on every GPU that loads it until the process exits.
+ * Limit: n_seqs <= 1024 (larger batches return BSA_ERR_INVALID_ARG);
+ * sequences longer than 8M tokens are rejected on the device as with
+ * bsa_prefill_fwd. The first call in a device's context looks up that
+ * context's address of the array (and sets the kernels' shared-memory
+ * limit); make that first call before any stream capture. All calls share
+ * the one array and each call rewrites it: calls whose GPU work overlaps
+ * (on different streams) race and must not be issued; calls on one stream
+ * are safe. Device-side errors (a malformed cu_seqlens, which leaves the
+ * outputs unwritten, or a pipeline time-out) accumulate in the array's
+ * status word until bsa_get_noalloc_status() reads and clears them.
  */
 bsa_status_t bsa_prefill_fwd_noalloc(const void *q, const void *k, const void *v,
                                      const int32_t *cu_seqlens, int32_t n_seqs,
@@ -192,6 +208,15 @@ bsa_status_t bsa_prefill_fwd_noalloc(const void *q, const void *k, const void *v
                                      int32_t causal, float lambda,
                                      bsa_dtype_t dtype, void *out, float *lse,
                                      uint32_t *skip_bitmap, bsa_stream_t stream);
+
+/*
+ * Status of the bsa_prefill_fwd_noalloc calls on the current device:
+ * synchronises `stream` (the stream those calls were made on), returns the
+ * device-side status they recorded since the last read (BSA_OK,
+ * BSA_ERR_BAD_SEQLENS or BSA_ERR_TIMEOUT) and clears it. Allocates nothing.
+ * BSA_OK if no such call was made in this context yet.
+ */
+bsa_status_t bsa_get_noalloc_status(bsa_stream_t stream);
 
 /*
  * Per-head dequantisation scales for the next BSA_FP8_E4M3 calls made on this
@@ -361,6 +386,15 @@ int32_t bsa_version(void);
  * this library is still running on any stream.
  */
 void bsa_release(void);
+
+/*
+ * Frees the scratch areas kept for `stream` on the current device
+ * (stream-ordered: work already enqueued on it finishes first). Call it
+ * before destroying a stream the library was used on; otherwise its scratch
+ * stays allocated until bsa_release(). No other host thread may be making
+ * calls on that stream at the same time. BSA_ERR_CUDA if a free fails.
+ */
+bsa_status_t bsa_release_stream(bsa_stream_t stream);
 
 #ifdef __cplusplus
 }

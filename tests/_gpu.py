@@ -16,7 +16,8 @@ import math
 import numpy as np
 import torch
 
-from oracle import layout, numerics, tile_walk
+import _oracle_pool
+from oracle import layout, tile_walk
 
 MARGIN_TOL = 1e-3
 O_MAX_BF16, O_MEAN_BF16 = 2e-2, 2e-3
@@ -83,19 +84,26 @@ def host(g):
     return g["out"].float().cpu().numpy().astype(np.float64), g["lse"].cpu().numpy().astype(np.float64)
 
 
-def sample_items(p, max_items=None, seed=0):
-    """All query tiles, or a deterministic sample: first / middle / last tile
-    of every sequence (random head) plus random tiles."""
+def sample_items(p, max_items=None, seed=0, tail_heads=4):
+    """All query tiles, or a deterministic sample of ``max_items``: the
+    first and middle tiles of every sequence (random heads), its last tile
+    (the sequence tail, the longest walk) for up to ``tail_heads`` heads,
+    then random tiles."""
     items = tile_walk.all_items(p.cu_seqlens, p.Hq)
     if max_items is None or len(items) <= max_items:
         return items
     rng = np.random.default_rng(seed)
-    pick = []
+    tails = max(1, min(tail_heads, max_items // (3 * p.n_seqs)))
+    pick = set()
     for s in range(p.n_seqs):
         n = layout.tiles(p.seqlens[s])
-        for i in sorted({0, n // 2, n - 1}):
-            pick.append((s, int(rng.integers(p.Hq)), i))
-    pick = sorted(set(pick))[:max_items]
+        pick.add((s, int(rng.integers(p.Hq)), 0))
+        pick.add((s, int(rng.integers(p.Hq)), n // 2))
+        for h in rng.choice(p.Hq, size=min(tails, p.Hq), replace=False):
+            pick.add((s, int(h), n - 1))
+    pick = sorted(pick)
+    if len(pick) > max_items:
+        pick = [pick[k] for k in sorted(rng.choice(len(pick), max_items, replace=False))]
     while len(pick) < max_items:
         it = items[int(rng.integers(len(items)))]
         if it not in pick:
@@ -103,58 +111,51 @@ def sample_items(p, max_items=None, seed=0):
     return sorted(pick)
 
 
-def _values(p, fp8, qrows, krows, heads_q, heads_kv):
-    """fp64 values of query rows ``qrows`` and key/value rows ``krows``."""
-    rows = (qrows, krows, krows)
-    if fp8 is None:
-        return tuple(numerics.bf16_to_f64(x[r][:, hs])
-                     for x, r, hs in zip((p.q, p.k, p.v), rows, (heads_q, heads_kv, heads_kv)))
-    out = []
-    for codes, scale, r, hs in zip(fp8[:3], fp8[3:], rows, (heads_q, heads_kv, heads_kv)):
-        out.append(numerics.e4m3_to_f64(codes[r][:, hs]) * np.asarray(scale, np.float64)[hs][None, :, None])
-    return tuple(out)
+# Sampled tiles of a full-size layer visit up to ~1000 key tiles each: past
+# this many tile visits in one comparison, the oracle runs on a process pool.
+POOL_VISITS = 20000
 
 
 def compare(p, g, items=None, fp8=None, check_bits=True):
     """Compare a GPU result with the oracle on ``items`` (all query tiles by
-    default); return a dict of metrics, asserting the tolerances."""
+    default); return a dict of metrics, asserting the tolerances. The count
+    of bits that differ within the decision margin (allowed) is printed."""
     cu = p.cu_seqlens
     cuk = p.cu_seqlens if p.cu_seqlens_k is None else p.cu_seqlens_k
     lam, causal = g["lam"], g["causal"]
-    G = p.Hq // p.Hkv
-    scale = 1.0 / math.sqrt(p.d)
+    items = tile_walk.all_items(cu, p.Hq) if items is None else list(items)
+    arrays = (p.q, p.k, p.v) if fp8 is None else tuple(fp8[:3])
+    scales = None if fp8 is None else tuple(fp8[3:])
+    gots, visits = [], 0
+    for item in items:
+        s, h, i = item
+        L, Lk = int(cu[s + 1] - cu[s]), int(cuk[s + 1] - cuk[s])
+        r1 = min(i * 128 + 128, L)
+        last = min((Lk - L + r1 - 1) // 128, layout.tiles(Lk) - 1) if causal else layout.tiles(Lk) - 1
+        row = layout.row_bits(g["bitmap"], cu, p.Hq, s, h, i, cuk)
+        assert not row[last + 1:].any(), f"bit set on an unvisited tile of {item}"
+        gots.append(row[:last + 1])
+        visits += last + 1
+    if visits > POOL_VISITS:
+        key = (p.name, p.total_tokens, id(arrays[0]), fp8 is not None)
+        refs = _oracle_pool.pool_references(key, arrays, scales, cu, cuk, p.Hq, p.Hkv, causal, lam,
+                                            items, gots)
+    else:
+        refs = [_oracle_pool.reference(arrays, scales, cu, cuk, p.Hq, p.Hkv, causal, lam, it, got)
+                for it, got in zip(items, gots)]
     bad_bits = near = 0
     o_max = o_sum = 0.0
     o_cnt = 0
     lse_max = 0.0
-    T = p.total_tokens
-    for item in (tile_walk.all_items(cu, p.Hq) if items is None else items):
+    for item, got, (want, mg, o_ref, lse_ref, last) in zip(items, gots, refs):
         s, h, i = item
-        a, L = int(cu[s]), int(cu[s + 1] - cu[s])
-        ak, Lk = int(cuk[s]), int(cuk[s + 1] - cuk[s])
-        off = Lk - L
-        r0, r1 = i * 128, min(i * 128 + 128, L)
-        last = min((off + r1 - 1) // 128, layout.tiles(Lk) - 1) if causal else layout.tiles(Lk) - 1
-        hi = min((last + 1) * 128, Lk)
-        # causal: keys past the last visited tile are never read, so the
-        # sequence truncated after it (queries keep their positions, so the
-        # chunk keeps the rows that end at key hi) walks identically
-        q_hi = hi - off if causal else L
-        q, k, v = _values(p, fp8, slice(a, a + q_hi), slice(ak, ak + hi), [h], [h // G])
-        sub_q, sub_k = [0, q_hi], [0, hi]
-        _, _, want, mg, _ = tile_walk.walk_one(q, k, v, sub_q, 1, 1, causal, lam, scale, (0, 0, i),
-                                               cu_seqlens_k=sub_k)
-        row = layout.row_bits(g["bitmap"], cu, p.Hq, s, h, i, cuk)
-        assert not row[last + 1:].any(), f"bit set on an unvisited tile of {item}"
-        got, want = row[:last + 1], want[:last + 1]
         for j in np.nonzero(got != want)[0]:
             if j < len(mg) and abs(mg[j]) < MARGIN_TOL:
                 near += 1
             else:
                 bad_bits += 1
-        o_ref, lse_ref, _, _, _ = tile_walk.walk_one(q, k, v, sub_q, 1, 1, causal, lam, scale,
-                                                     (0, 0, i), replay=got, cu_seqlens_k=sub_k)
-        r0, r1 = a + r0, a + r1
+        a, L = int(cu[s]), int(cu[s + 1] - cu[s])
+        r0, r1 = a + i * 128, a + min(i * 128 + 128, L)
         o_gpu = g["out"][r0:r1, h].float().cpu().numpy().astype(np.float64)
         l_gpu = g["lse"][h, r0:r1].cpu().numpy().astype(np.float64)
         d = np.abs(o_gpu - o_ref)
@@ -163,8 +164,9 @@ def compare(p, g, items=None, fp8=None, check_bits=True):
         o_sum += float(d.sum())
         o_cnt += d.size
         lse_max = max(lse_max, float(np.abs(l_gpu - lse_ref).max()))
-    res = dict(bad_bits=bad_bits, near_margin=near, o_max=o_max, o_mean=o_sum / max(o_cnt, 1),
-               lse_max=lse_max, values=o_cnt)
+    res = dict(items=len(items), tile_visits=visits, bad_bits=bad_bits, near_margin=near,
+               o_max=o_max, o_mean=o_sum / max(o_cnt, 1), lse_max=lse_max, values=o_cnt)
+    print(f"parity {p.name} lambda={lam} causal={causal} fp8={fp8 is not None}: {res}")
     if check_bits:
         assert bad_bits == 0, f"{bad_bits} skip bits differ outside the 1e-3 margin: {res}"
     if fp8 is None:

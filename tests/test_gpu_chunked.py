@@ -61,7 +61,7 @@ def test_chunked_full_size_sampled():
     p = gi.chunk(gi.config("C1"), [8192])
     g = _gpu.run(p, lam=0.01)
     assert bool(torch.isfinite(g["out"]).all())
-    print(_gpu.compare(p, g, items=_gpu.sample_items(p, 12, seed=3)))
+    _gpu.compare(p, g, items=_gpu.sample_items(p, 12, seed=3))
 
 
 def test_chunked_rejects_fewer_keys_than_queries():

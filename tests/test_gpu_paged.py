@@ -152,3 +152,47 @@ def test_paged_fp8_equals_packed():
     g = dict(out=out, lse=lse, bitmap=bm[:nw].cpu().numpy().view(np.uint32), lam=0.05, causal=True)
     assert np.array_equal(g["bitmap"], ref["bitmap"])
     _gpu.compare(p, g, fp8=f8)
+
+
+def test_paged_128k_chunk_as_benched():
+    """The bench's paged leg: the last 8192 queries of the 128K layer against
+    all 131072 keys, K/V scattered over a shuffled pool of 1024 pages (page j
+    of the sequence is pool page perm[j]). Equal bit for bit to the packed
+    chunked call, and matching the oracle on sampled query tiles (the last
+    tiles of several heads included)."""
+    b = _gpu.bsa()
+    base = gi.config("C2")
+    p = gi.chunk(base, [8192])
+    T, Hq, Hkv, d = base.total_tokens, base.Hq, base.Hkv, base.d
+    n_pages = T // 128
+    perm = np.random.default_rng(0).permutation(n_pages).astype(np.int32)
+    k, v = _gpu.to_dev_bf16(base.k), _gpu.to_dev_bf16(base.v)
+    kpool = torch.empty_like(k)
+    vpool = torch.empty_like(v)
+    pd = torch.from_numpy(perm).cuda()
+    kpool.view(n_pages, 128, Hkv, d)[pd.long()] = k.view(n_pages, 128, Hkv, d)
+    vpool.view(n_pages, 128, Hkv, d)[pd.long()] = v.view(n_pages, 128, Hkv, d)
+    q = _gpu.to_dev_bf16(p.q)
+    cq = torch.tensor([0, 8192], dtype=torch.int32, device="cuda")
+    ck = torch.from_numpy(base.cu_seqlens).cuda()
+    nw = b.skip_bitmap_words_chunked(p.cu_seqlens, base.cu_seqlens, Hq)
+    res = []
+    for paged in (True, False):
+        out = torch.full((8192, Hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((Hq, 8192), float("nan"), dtype=torch.float32, device="cuda")
+        bm = torch.full((nw,), -1, dtype=torch.int32, device="cuda")
+        if paged:
+            st = b.prefill_fwd_paged(q, kpool, vpool, pd.view(1, n_pages), n_pages, n_pages, cq, ck,
+                                     1, Hq, Hkv, d, 1, 0.01, b.BSA_BF16, out, lse, bm)
+        else:
+            st = b.prefill_fwd_chunked(q, k, v, cq, ck, 1, Hq, Hkv, d, 1, 0.01, b.BSA_BF16, out,
+                                       lse, bm)
+        b.check(st, "paged" if paged else "chunked")
+        torch.cuda.synchronize()
+        b.check(b.get_device_status(), "device status")
+        res.append(dict(out=out, lse=lse, bitmap=bm.cpu().numpy().view(np.uint32), lam=0.01,
+                        causal=True))
+    g, ref = res
+    assert torch.equal(g["out"], ref["out"]) and torch.equal(g["lse"], ref["lse"])
+    assert np.array_equal(g["bitmap"], ref["bitmap"])
+    _gpu.compare(p, g, items=_gpu.sample_items(p, 32, seed=5))

@@ -90,3 +90,78 @@ def test_noalloc_matches_allocating_call_twice_in_a_row():
     p, lam, ins, ref, first, second = prepared[0]
     _agree(p, ref, second)
     _agree(p, ref, warm)
+    assert b.get_noalloc_status() == 0
+
+
+@pytest.mark.gpu
+def test_noalloc_fp8_and_a_thousand_sequences():
+    """The FP8 branch (scales registered on the calling thread) and a batch
+    of about a thousand short sequences, where the fixed area's sequence
+    order and bitmap-offset tables are nearly full; each against the
+    allocating call, twice in a row."""
+    import test_gpu_fp8
+    from gen import inputs as gi
+    b = _gpu.bsa()
+    b.get_noalloc_status()   # start from a clear status word
+    # FP8
+    p = _cases.small_problem("gqa_ragged")
+    f8 = [test_gpu_fp8.gpu_quantize(x) for x in (p.q, p.k, p.v)]
+    codes = [torch.from_numpy(c).cuda() for c, _ in f8]
+    scales = [torch.from_numpy(np.asarray(s, np.float32)).cuda() for _, s in f8]
+    cu = torch.from_numpy(p.cu_seqlens.astype(np.int32)).cuda()
+    b.check(b.set_fp8_scales(*scales), "scales")
+    try:
+        res = []
+        for fn in (b.prefill_fwd, b.prefill_fwd_noalloc, b.prefill_fwd_noalloc):
+            outs = _outputs(p)
+            b.check(fn(codes[0], codes[1], codes[2], cu, p.n_seqs, p.Hq, p.Hkv, p.d, 1, 0.01,
+                       b.BSA_FP8_E4M3, *outs), fn.__name__)
+            res.append(outs)
+        torch.cuda.synchronize()
+    finally:
+        b.check(b.set_fp8_scales(None, None, None), "clear scales")
+    assert b.get_noalloc_status() == 0
+    for got in res[1:]:
+        o_ref, l_ref, b_ref = res[0]
+        o_got, l_got, b_got = got
+        assert float((o_got.float() - o_ref.float()).abs().max()) <= _gpu.O_MAX_FP8
+        assert float((l_got - l_ref).abs().max()) <= _gpu.LSE_TOL
+        assert torch.equal(b_got, b_ref)
+    # 1000 sequences of 1 .. 300 tokens
+    lengths = np.random.default_rng(9).integers(1, 301, 1000).tolist()
+    pm = gi.small("many", lengths, Hq=2, Hkv=1, seed=9)
+    ins = _args(pm)
+    ref = _outputs(pm)
+    _call(b.prefill_fwd, pm, 0.01, ins, ref)
+    got = [_outputs(pm), _outputs(pm)]
+    for outs in got:
+        _call(b.prefill_fwd_noalloc, pm, 0.01, ins, outs)
+    torch.cuda.synchronize()
+    assert b.get_noalloc_status() == 0
+    for outs in got:
+        _agree(pm, ref, outs)
+
+
+@pytest.mark.gpu
+def test_noalloc_device_errors_reach_its_status_reader():
+    """A decreasing cu_seqlens is caught on the device: nothing is written,
+    bsa_get_noalloc_status reports BSA_ERR_BAD_SEQLENS once (reading clears
+    it), and the next good call is correct."""
+    b = _gpu.bsa()
+    b.get_noalloc_status()
+    p = _cases.small_problem("gqa_ragged")
+    q, k, v, _ = _args(p)
+    bad = torch.tensor([0, 500, 300, 400], dtype=torch.int32, device="cuda")
+    out = torch.full((p.total_tokens, p.Hq, p.d), 7.0, dtype=torch.bfloat16, device="cuda")
+    st = b.prefill_fwd_noalloc(q, k, v, bad, 3, p.Hq, p.Hkv, p.d, 1, 0.01, b.BSA_BF16, out, None, None)
+    assert st == 0   # the host cannot see device data; the prologue checks it
+    assert b.get_noalloc_status() == 6
+    assert b.get_noalloc_status() == 0
+    assert bool((out == 7.0).all())
+    ins = _args(p)
+    ref, first = _outputs(p), _outputs(p)
+    _call(b.prefill_fwd, p, 0.01, ins, ref)
+    _call(b.prefill_fwd_noalloc, p, 0.01, ins, first)
+    torch.cuda.synchronize()
+    assert b.get_noalloc_status() == 0
+    _agree(p, ref, first)
