@@ -36,10 +36,12 @@
 // Per key tile j and query slot s the softmax warpgroup loads S_s from TMEM,
 // masks the diagonal / tail and computes P = exp2(S c - m_ref) into TMEM:
 // on the first tile after the row max, later in one pass against the current
-// reference, with a lazy O rescale (and a second pass) only for a row whose
-// max grows by more than 2^8; then it posts P-ready. The MMA warp issues
-// O_s += P_s V_j before the next S_s, so the tensor pipe's in-order execution
-// protects P until it has been read.
+// reference (scale-and-subtract and the row sum on pairs of scores with the
+// packed f32x2 FMA / add), with a lazy O rescale (and a second pass) only for
+// a row whose max grows by more than 2^8; then each warp posts its 32 rows
+// to the P-ready barrier. The MMA warp issues O_s += P_s V_j before the next
+// S_s, so the tensor pipe's in-order execution protects P until it has been
+// read.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -271,7 +273,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   const uint64_t limit = p.wait_limit_ns;
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < B_COUNT; ++b) mbar_init(&bar[b], 1);
+    for (int b = 0; b < B_COUNT; ++b)
+      mbar_init(&bar[b], (b == B_PRDY || b == B_PRDY + 1) ? 4 : 1);   // P-ready: one arrival per warp
     fence_mbar_init();
     abort_sh = 0;
     for (int k = 0; k < 20; ++k) ctr_sh[k] = 0u;
@@ -446,7 +449,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       if (h >= 0) {
         const int row = threadIdx.x & 127;   // = TMEM lane
         uint32_t sc = ctr_sh[12 + 4 * slot], pvc = ctr_sh[13 + 4 * slot];
-        const uint32_t barid = 1 + slot;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + kColS + slot * 128 + lane_off;
         const uint32_t tO = tmem + kColO + slot * 128 + lane_off;
@@ -464,7 +466,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         bool have_kept = false;
 
         for (int j = 0; j <= last; ++j) {
-          if (!mbar_wait(&bar[B_SF + slot], sc & 1, limit, kSpinSoftmax)) abort_sh = 1;
+          if (!abort_sh && !mbar_wait(&bar[B_SF + slot], sc & 1, limit, kSpinSoftmax)) abort_sh = 1;
           ++sc;
           tc_fence_after();
           const int doff = doff0 - j * kTile;   // row r sees columns <= r + doff
@@ -476,7 +478,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             // taken; only when a row's max outgrows the reference by more than
             // 2^8 is O rescaled and the tile's P recomputed (S is still intact:
             // P is stored at the end).
-            if (!mbar_wait(&bar[B_PV + slot], pvc & 1, limit)) abort_sh = 1;
+            if (!abort_sh && !mbar_wait(&bar[B_PV + slot], pvc & 1, limit)) abort_sh = 1;
             ++pvc;
             tc_fence_after();
             constexpr int kPk = FP8 ? 8 : 16;   // packed words per 32-key chunk
@@ -500,13 +502,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
                 }
                 if (diag || tailt) mask_chunk(v, ch, diag, tailt, row, doff, j * kTile, Lk);
                 float pv[32];
+                const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(nm, nm);
+                uint64_t ps2[4];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                  const float x = __uint_as_float(v[e]);
-                  if (track) tmx[e & 3] = fmaxf(tmx[e & 3], x);
-                  pv[e] = ex2_approx(fmaf(x, c, nm));
-                  psum[e & 7] += pv[e];
+                for (int k = 0; k < 4; ++k) ps2[k] = f2_pack(psum[2 * k], psum[2 * k + 1]);
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                  const float x0 = __uint_as_float(v[e]), x1 = __uint_as_float(v[e + 1]);
+                  if (track) tmx[(e >> 1) & 3] = max3f(tmx[(e >> 1) & 3], x0, x1);
+                  float y0, y1;
+                  f2_unpack(f2_fma(f2_pack(x0, x1), c2, nm2), y0, y1);
+                  pv[e] = ex2_approx(y0);
+                  pv[e + 1] = ex2_approx(y1);
+                  ps2[(e >> 1) & 3] = f2_add(ps2[(e >> 1) & 3], f2_pack(pv[e], pv[e + 1]));
                 }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) f2_unpack(ps2[k], psum[2 * k], psum[2 * k + 1]);
 #pragma unroll
                 for (int k = 0; k < kPk; ++k) {
                   if (FP8)
@@ -549,12 +560,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             tmem_wait_st();
             l += ((psum[0] + psum[1]) + (psum[2] + psum[3])) + ((psum[4] + psum[5]) + (psum[6] + psum[7]));
             tc_fence_before();
-            named_bar_sync(barid, 128);
-            if (abort_sh) {   // read after the barrier: uniform over the warpgroup
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_PRDY + slot]);   // this warp's 32 rows of P
+            if (abort_sh) {
               ok = false;
               break;
             }
-            if (row == 0) mbar_arrive(&bar[B_PRDY + slot]);
             if (row == 0 && brow && (((j & 31) == 31) || j == last)) {
               brow[j >> 5] = word;
               word = 0;
@@ -658,12 +669,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             tmem_wait_st();
             l += sum;
             tc_fence_before();
-            named_bar_sync(barid, 128);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_PRDY + slot]);
             if (abort_sh) {
               ok = false;
               break;
             }
-            if (row == 0) mbar_arrive(&bar[B_PRDY + slot]);
             have_kept = true;
           }
           if (row == 0 && brow && (((j & 31) == 31) || j == last)) {

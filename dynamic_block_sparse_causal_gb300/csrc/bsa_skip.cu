@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kSkipThreads, 1) skip_kernel(const __grid_cons
     const int s = I[1], kvh = I[2], h0 = I[3], h1 = I[4], qi = I[5], a = I[6], L = I[7];
     const int ak = I[8], Lk = I[9];
     const int off = Lk - L;   // query row r sits at key position off + r
-    const int nq = (L + kTile - 1) / kTile, nk = (Lk + kTile - 1) / kTile;
+    const int nk = (Lk + kTile - 1) / kTile;
     const int qlast = min(qi * kTile + kTile, L) - 1;
     const int last = p.causal ? min((off + qlast) / kTile, nk - 1) : nk - 1;
     const int npairs = (last + 2) >> 1;
@@ -419,17 +419,13 @@ __global__ void __launch_bounds__(kSkipThreads, 1) skip_kernel(const __grid_cons
   for (int it = 0;; ++it) {
     const int *I = item_sh[it & 1];
     if (!I[0] || abort_sh) break;
-    const int s = I[1], kvh = I[2], h0 = I[3], h1 = I[4], qi = I[5], a = I[6], L = I[7];
-    const int ak = I[8], Lk = I[9];
+    const int s = I[1], kvh = I[2], h0 = I[3], h1 = I[4], qi = I[5], L = I[7];
+    const int Lk = I[9];
     const int off = Lk - L;   // query row r sits at key position off + r
     const int nq = (L + kTile - 1) / kTile, nk = (Lk + kTile - 1) / kTile;
     const int qlast = min(qi * kTile + kTile, L) - 1;
     const int last = p.causal ? min((off + qlast) / kTile, nk - 1) : nk - 1;
     const int npairs = (last + 2) >> 1;
-    const bool has1 = h1 >= 0;
-    auto kv_row = [&](int j) -> int {
-      return p.page_table ? p.page_table[(size_t)s * p.max_pages + j] * kTile : ak + j * kTile;
-    };
     bool ok = true;
     {
       // -------------------------------------------------- slot warpgroups

@@ -66,6 +66,17 @@ def small_problem(key: str) -> gi.Problem:
     raise KeyError(key)
 
 
+def full_problem(name: str, sink: float = 4.0) -> gi.Problem:
+    """A full-size workload (C1, C2, C3; C4 is C2's values, quantised by the
+    FP8 tests), generated once per test session and shared by every module."""
+    return _full("C2" if name == "C4" else name, sink)
+
+
+@functools.lru_cache(maxsize=4)
+def _full(name: str, sink: float) -> gi.Problem:
+    return gi.config(name, sink=sink)
+
+
 def f64(bits):
     w = np.asarray(bits, np.uint16).astype(np.uint32) << np.uint32(16)
     return w.view(np.float32).astype(np.float64)

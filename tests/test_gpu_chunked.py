@@ -58,7 +58,7 @@ def test_aligned_chunk_equals_whole_sequence_rows():
 
 def test_chunked_full_size_sampled():
     """The last 8192 queries of the 32K Llama-shaped layer against all its keys."""
-    p = gi.chunk(gi.config("C1"), [8192])
+    p = gi.chunk(_cases.full_problem("C1"), [8192])
     g = _gpu.run(p, lam=0.01)
     assert bool(torch.isfinite(g["out"]).all())
     _gpu.compare(p, g, items=_gpu.sample_items(p, 12, seed=3))

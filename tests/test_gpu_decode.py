@@ -85,7 +85,7 @@ def test_decode_max_seqlen_larger_than_needed():
 
 def test_decode_full_layer_one_query():
     """One new query at the end of the 128K Llama-shaped layer, all 32 heads."""
-    p = gi.chunk(gi.config("C2"), [1])
+    p = gi.chunk(_cases.full_problem("C2"), [1])
     for lam in (0.005, 0.0):
         g, st = run_decode(p, lam)
         assert st == 0

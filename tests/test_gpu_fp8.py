@@ -66,7 +66,7 @@ def test_fp8_attention(key, lam, causal):
 
 
 def test_fp8_full_size_sampled():
-    p = gi.config("C1")
+    p = _cases.full_problem("C1")
     f8 = quantized(p)
     g = _gpu.run(p, lam=0.01, fp8=f8)
     assert bool(torch.isfinite(g["out"]).all())
@@ -78,7 +78,7 @@ _C4 = {}
 
 def _c4():
     if not _C4:
-        p = gi.config("C4")
+        p = _cases.full_problem("C4")
         _C4["p"], _C4["f8"] = p, quantized(p)
     return _C4["p"], _C4["f8"]
 

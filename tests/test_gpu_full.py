@@ -9,22 +9,19 @@ tiles zero, the first tile of every row kept.
 """
 from __future__ import annotations
 
-import functools
-
 import numpy as np
 import pytest
 import torch
 
+import _cases
 import _gpu
-from gen import inputs as gi
 from oracle import layout
 
 pytestmark = pytest.mark.gpu
 
 
-@functools.lru_cache(maxsize=2)
 def problem(name, sink=4.0):
-    return gi.config(name, sink=sink)
+    return _cases.full_problem(name, sink)
 
 
 def whole_output_properties(p, g):
@@ -44,9 +41,13 @@ def whole_output_properties(p, g):
 
 # every configuration bench.py times: the 32K layer, the 128K layer at each
 # lambda of its sweep, and the packed batch with and without skipping
+
+
 @pytest.mark.parametrize("name,lam,n_items", [("C1", 0.01, 24), ("C1", 0.0, 8), ("C3", 0.01, 32),
                                               ("C3", 0.0, 32), ("C2", 0.0, 32), ("C2", 1e-3, 32),
                                               ("C2", 0.01, 40), ("C2", 0.05, 32)])
+
+
 def test_full_size_sampled(name, lam, n_items):
     p = problem(name)
     g = _gpu.run(p, lam=lam)

@@ -132,7 +132,7 @@ def test_empty_sequence_and_window_longer_than_sequence():
 def test_full_size_mass_and_sampled_heads():
     """The 128K Llama-shaped layer: every head's scores add up to 1/128, and
     four heads (one per KV group pair) match the oracle."""
-    p = gi.config("C2")
+    p = _cases.full_problem("C2")
     sc, mn, st = run_importance(p, 64)
     assert st == 0
     s = sc.cpu().numpy().astype(np.float64)

@@ -161,7 +161,7 @@ def test_paged_128k_chunk_as_benched():
     chunked call, and matching the oracle on sampled query tiles (the last
     tiles of several heads included)."""
     b = _gpu.bsa()
-    base = gi.config("C2")
+    base = _cases.full_problem("C2")
     p = gi.chunk(base, [8192])
     T, Hq, Hkv, d = base.total_tokens, base.Hq, base.Hkv, base.d
     n_pages = T // 128
