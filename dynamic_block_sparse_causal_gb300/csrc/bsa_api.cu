@@ -206,8 +206,13 @@ bsa_status_t prefill(const void *q, const void *k, const void *v, const int32_t 
   std::lock_guard<std::mutex> lock(ss->mu);
   Workspace *ws = nullptr;
   if ((st = scratch_for(ss, stream, layout.bytes, &ws)) != BSA_OK) return st;
-  if (bsa::launch_prologue(cu_seqlens, cu_seqlens_k, n_seqs, Hq, Hkv, causal, page_table,
-                           max_pages, num_pages, ws, layout, tmpl, stream) != cudaSuccess)
+  // two query heads of a group per work item (they share every K tile)
+  const bool skip = lambda > 0.f;
+  const int heads = 2;
+  const int group = Hq / Hkv, items_per_group = (group + heads - 1) / heads;
+  if (bsa::launch_prologue(cu_seqlens, cu_seqlens_k, n_seqs, Hq, Hkv, items_per_group, causal,
+                           page_table, max_pages, num_pages, ws, layout, tmpl, stream) !=
+      cudaSuccess)
     return BSA_ERR_CUDA;
 
   char *base = reinterpret_cast<char *>(ws);
@@ -228,16 +233,17 @@ bsa_status_t prefill(const void *q, const void *k, const void *v, const int32_t 
   p.v_scale = fp8 ? t_v_scale : nullptr;
   p.Hq = Hq;
   p.Hkv = Hkv;
-  p.group = Hq / Hkv;
-  p.pairs_per_group = (p.group + 1) / 2;
+  p.group = group;
+  p.heads_per_item = heads;
+  p.items_per_group = items_per_group;
   p.causal = causal;
   p.c = (float)(1.0 / std::sqrt((double)d) * 1.4426950408889634);
   p.log2_lambda = lambda > 0.f ? (float)std::log2((double)lambda) : -INFINITY;
   p.wait_limit_ns = t_wait_limit_ns;
   p.debug_drop_k_load = t_drop_k_load;
   // lambda > 0: decisions first, then the kept tiles; lambda = 0: one dense pass
-  const cudaError_t e = lambda > 0.f ? bsa::launch_skip(p, fp8, info->sm_count, stream)
-                                     : bsa::launch_forward(p, fp8, info->sm_count, stream);
+  const cudaError_t e = skip ? bsa::launch_skip(p, fp8, info->sm_count, stream)
+                             : bsa::launch_forward(p, fp8, info->sm_count, stream);
   if (e != cudaSuccess) return BSA_ERR_CUDA;
   return BSA_OK;
 }

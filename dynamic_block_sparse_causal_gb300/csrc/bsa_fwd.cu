@@ -65,7 +65,7 @@ __device__ __forceinline__ int q_tiles(const int32_t *cu, int s) {
 
 __global__ void __launch_bounds__(1024)
 prologue_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ cuk, int n_seqs,
-                int Hq, int Hkv, int causal, const int32_t *__restrict__ page_table,
+                int Hq, int Hkv, int items_per_group, int causal, const int32_t *__restrict__ page_table,
                 int max_pages, int num_pages, Workspace *ws, int32_t *seq_sorted,
                 int64_t *seq_bitmap_off, int32_t *level_start,
                 const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -98,11 +98,10 @@ prologue_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ cuk,
   }
   __syncthreads();
   const int maxn = s_maxn;
-  const int group = Hq / Hkv;
   // work items are ordered KV head by KV head (so CTAs running at the same time
   // stream the same head's K tiles through L2), and within a head longest
   // query tile first; U = items per (sequence, query tile) within one head
-  const long long U = (group + 1) / 2;
+  const long long U = items_per_group;
   bool bad = s_bad || maxn > kMaxLevels;
   if (!bad) {
     // longest first (query tiles), ties by sequence index
@@ -159,13 +158,14 @@ prologue_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ cuk,
 }
 
 cudaError_t launch_prologue(const int32_t *cu_seqlens, const int32_t *cu_seqlens_k, int n_seqs,
-                            int Hq, int Hkv, int causal, const int32_t *page_table,
+                            int Hq, int Hkv, int items_per_group, int causal,
+                            const int32_t *page_table,
                             int max_pages, int num_pages, Workspace *ws,
                             const WorkspaceLayout &layout, const CUtensorMap tmpl[3],
                             cudaStream_t stream) {
   char *base = reinterpret_cast<char *>(ws);
   prologue_kernel<<<1, 1024, 0, stream>>>(
-      cu_seqlens, cu_seqlens_k, n_seqs, Hq, Hkv, causal, page_table, max_pages, num_pages, ws,
+      cu_seqlens, cu_seqlens_k, n_seqs, Hq, Hkv, items_per_group, causal, page_table, max_pages, num_pages, ws,
       reinterpret_cast<int32_t *>(base + layout.seq_sorted),
       reinterpret_cast<int64_t *>(base + layout.seq_bitmap_off),
       reinterpret_cast<int32_t *>(base + layout.level_start), tmpl[0], tmpl[1], tmpl[2]);

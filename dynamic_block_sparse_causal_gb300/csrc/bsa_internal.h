@@ -64,7 +64,8 @@ struct FwdParams {
   const float *k_scale;
   const float *v_scale;
   int32_t Hq, Hkv, group;    // group = Hq / Hkv
-  int32_t pairs_per_group;   // ceil(group / 2): query heads are handled two at a time
+  int32_t heads_per_item;    // query heads of one group per work item (2: they share K tiles)
+  int32_t items_per_group;   // ceil(group / heads_per_item)
   int32_t causal;
   float c;                   // softmax scale * log2(e)
   float log2_lambda;         // -inf when skipping is off
@@ -75,8 +76,10 @@ struct FwdParams {
 // Host-side launchers (bsa_fwd.cu).
 // page_table / max_pages / num_pages: paged K/V (page = one 128-token tile);
 // page_table == nullptr for packed K/V, whose token extent the prologue patches.
+// items_per_group: work items per (sequence, KV head, query tile).
 cudaError_t launch_prologue(const int32_t *cu_seqlens, const int32_t *cu_seqlens_k, int n_seqs,
-                            int Hq, int Hkv, int causal, const int32_t *page_table,
+                            int Hq, int Hkv, int items_per_group, int causal,
+                            const int32_t *page_table,
                             int max_pages, int num_pages, Workspace *ws,
                             const WorkspaceLayout &layout, const CUtensorMap tmpl[3],
                             cudaStream_t stream);
@@ -88,6 +91,7 @@ cudaError_t prepare_forward();   // per device: opt in to the shared-memory size
 // decisions, then the kept tiles.
 cudaError_t launch_skip(const FwdParams &p, bool fp8, int num_ctas, cudaStream_t stream);
 cudaError_t prepare_skip();
+
 
 // FP8 scales registered on the calling thread (bsa_api.cu).
 void current_fp8_scales(const float **q, const float **k, const float **v);

@@ -156,7 +156,12 @@ extern "C" bsa_status_t bsa_prefill_fwd_noalloc(
   // the status word keeps its bits until bsa_get_noalloc_status reads them;
   // everything else the prologue rewrites
   bsa::Workspace *ws = static_cast<bsa::Workspace *>(s->scratch);
-  if (bsa::launch_prologue(cu_seqlens, cu_seqlens, n_seqs, Hq, Hkv, causal, nullptr, 0, 0, ws, kLayout, tmpl, stream) != cudaSuccess)
+  // the same kernels as bsa_prefill_fwd (two query heads per work item)
+  const bool skip = lambda > 0.f;
+  const int heads = 2;
+  const int group = Hq / Hkv, items_per_group = (group + heads - 1) / heads;
+  if (bsa::launch_prologue(cu_seqlens, cu_seqlens, n_seqs, Hq, Hkv, items_per_group, causal,
+                           nullptr, 0, 0, ws, kLayout, tmpl, stream) != cudaSuccess)
     return BSA_ERR_CUDA;
 
   char *base = static_cast<char *>(s->scratch);
@@ -177,15 +182,16 @@ extern "C" bsa_status_t bsa_prefill_fwd_noalloc(
   p.v_scale = vs;
   p.Hq = Hq;
   p.Hkv = Hkv;
-  p.group = Hq / Hkv;
-  p.pairs_per_group = (p.group + 1) / 2;
+  p.group = group;
+  p.heads_per_item = heads;
+  p.items_per_group = items_per_group;
   p.causal = causal;
   p.c = (float)(1.0 / std::sqrt((double)d) * 1.4426950408889634);
   p.log2_lambda = lambda > 0.f ? (float)std::log2((double)lambda) : -INFINITY;
   p.wait_limit_ns = 2000000000ull;
   p.debug_drop_k_load = -1;
-  const cudaError_t e = lambda > 0.f ? bsa::launch_skip(p, fp8, s->sm_count, stream)
-                                     : bsa::launch_forward(p, fp8, s->sm_count, stream);
+  const cudaError_t e = skip ? bsa::launch_skip(p, fp8, s->sm_count, stream)
+                             : bsa::launch_forward(p, fp8, s->sm_count, stream);
   if (e != cudaSuccess) return BSA_ERR_CUDA;
   return BSA_OK;
 }

@@ -78,17 +78,17 @@ __device__ __forceinline__ void fetch_item(const FwdParams &p, int total_items, 
     else
       lo = mid + 1;
   }
-  const int U = p.pairs_per_group;
+  const int U = p.items_per_group;
   const int r = kr - p.level_start[lo];
   const int s = p.seq_sorted[r / U];
   const int pp = r % U;
-  const int h0 = kvh * p.group + 2 * pp;
+  const int h0 = kvh * p.group + p.heads_per_item * pp;
   const int a = p.cu_seqlens[s], ak = p.cu_seqlens_k[s];
   dst[0] = 1;
   dst[1] = s;
   dst[2] = kvh;
   dst[3] = h0;
-  dst[4] = (2 * pp + 1 < p.group) ? h0 + 1 : -1;
+  dst[4] = (p.heads_per_item == 2 && 2 * pp + 1 < p.group) ? h0 + 1 : -1;
   dst[5] = lo;
   dst[6] = a;
   dst[7] = p.cu_seqlens[s + 1] - a;
