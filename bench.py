@@ -11,8 +11,13 @@ kept tiles) with the measured dense bf16 peak; ``cpu_baseline`` times the
 fp64 CPU oracle on a bounded sample of the same layer.
 
 ``--impl reference`` times the CPU oracle alone (the reference arm).
-Multi-GPU: one process per GPU (torchrun), each running the same layer
-(weak scaling, no collective on the data path).
+Multi-GPU: one process per GPU (torchrun). By default the layer's KV heads
+are split over the ranks (rank r computes KV heads [r Hkv / N, (r + 1) Hkv / N)
+and their query heads from contiguous copies made before timing; strong
+scaling, ``value`` = the whole layer's FLOPs over the slowest rank's time);
+``--split replicas`` runs the whole layer on every rank (weak scaling). No
+collective is on the data path: the ranks meet only for the barriers and the
+max-over-ranks of the times.
 """
 from __future__ import annotations
 
@@ -416,9 +421,15 @@ def gpu_arm(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
     bsa.lib()
     p = gi.config(args.config, seed=args.seed, lam=args.lam, sink=args.sink)
+    split = world > 1 and args.split == "heads"
+    layer_Hq = p.Hq
+    if split:   # this rank's KV heads and their query heads (contiguous copies)
+        p = gi.split_heads(p, rank, world)
     seqlens = [int(x) for x in p.seqlens]
     T, Hq, Hkv, d = p.total_tokens, p.Hq, p.Hkv, p.d
     dflops = dense_flops(seqlens, Hq, d)
+    # FLOPs of the whole job: the layer once (split), or once per rank (replicas)
+    job_flops = dense_flops(seqlens, layer_Hq, d) if split else dflops * world
     stream = torch.cuda.current_stream()
 
     def upload(bits):
@@ -464,7 +475,7 @@ def gpu_arm(args, rank, world, local_rank):
     skipped = popcount(bm.cpu().numpy())
     ctiles = causal_tiles(seqlens, Hq)
     xflops = executed_flops(seqlens, Hq, skipped, d)
-    value = dflops * world / (ms * 1e-3) / 1e12
+    value = job_flops / (ms * 1e-3) / 1e12
 
     peaks = {}
     try:
@@ -788,13 +799,13 @@ def gpu_arm(args, rank, world, local_rank):
         ms_serial = run_e2e(max(2, args.steps // 2), False)
         h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + hcu.numel() * 4
         d2h = hres[0][0].numel() * 2 + hres[0][1].numel() * 4 + hres[0][2].numel() * 4
-        e2e = {"value": round(dflops * world / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        e2e = {"value": round(job_flops / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                "ms_per_step": round(ms_e2e, 3), "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
                "overlap": "upload of step i+1 and download of step i-1 on copy streams during the "
                           "forward of step i (two buffer sets); first upload and last download timed",
                "serial_ms_per_step": round(ms_serial, 3),
-               "serial_value": round(dflops * world / (ms_serial * 1e-3) / 1e12, 2)}
+               "serial_value": round(job_flops / (ms_serial * 1e-3) / 1e12, 2)}
         bsa.check(bsa.get_device_status(stream), "device status")
         del dbuf, hres
 
@@ -810,12 +821,14 @@ def gpu_arm(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
         "ms_per_step_mean": round(ms_mean, 3), "timing": "median of per-step CUDA-event times",
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "strong" if split else "weak", "vs_baseline": None,
+        "dtype": "bf16",
         "data": "synthetic (seeded generator: sink + local-window bias, Llama-3-8B attention shape)",
         "config": {"workload": WORKLOADS.get(args.config, args.config), "name": args.config,
                    "tokens": T, "Hq": Hq, "Hkv": Hkv, "d": d, "lambda": args.lam, "causal": True,
                    "sink": args.sink,
-                   "parallelism": f"replicas x{world}",
+                   "parallelism": (f"kv-head split x{world} (this rank: {Hkv} KV heads, {Hq} query heads)"
+                                   if split else f"replicas x{world}"),
                    "l2": "inputs larger than L2 (q/out 1.07 GB each, k/v 0.27 GB each); no flush"},
         "skip_fraction": round(skipped / ctiles, 5), "executed_tflop_per_step": round(xflops / 1e12, 3),
         "dense_equiv_tflop_per_step": round(dflops / 1e12, 3),
@@ -877,6 +890,9 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--sink", type=float, default=4.0,
                     help="sink strength of the input recipe (4.0; smaller keeps more tiles)")
+    ap.add_argument("--split", default="heads", choices=["heads", "replicas"],
+                    help="with several GPUs: split the layer's KV heads over the ranks (default) "
+                         "or run the whole layer on every rank")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

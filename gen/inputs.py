@@ -189,3 +189,24 @@ def small(name: str, lengths, Hq: int = 4, Hkv: int = 2, seed: int = 0, lam: flo
     """A parity-sized problem with the same recipe and a shorter window period."""
     return packed(name, lengths, Hq, Hkv, seed, causal=causal, lam=lam, sink=sink,
                   window=window, window_period=window_period, window_len=window_len)
+
+
+def head_range(Hkv: int, world: int, rank: int) -> tuple:
+    """KV heads [lo, hi) of rank ``rank`` when a layer's heads are split over
+    ``world`` processes: contiguous, sizes differing by at most one."""
+    if not 0 <= rank < world or world > Hkv:
+        raise ValueError("need 0 <= rank < world <= Hkv")
+    return rank * Hkv // world, (rank + 1) * Hkv // world
+
+
+def split_heads(p: Problem, rank: int, world: int) -> Problem:
+    """The part of ``p`` one process computes when the KV heads are split over
+    ``world`` processes: KV heads ``head_range`` and the query heads of their
+    groups, as contiguous arrays (query head h of the piece is query head
+    lo * G + h of the layer). Sequences, lengths and values are unchanged."""
+    G = p.Hq // p.Hkv
+    lo, hi = head_range(p.Hkv, world, rank)
+    return Problem(f"{p.name}_heads{lo}-{hi}", np.ascontiguousarray(p.q[:, lo * G:hi * G]),
+                   np.ascontiguousarray(p.k[:, lo:hi]), np.ascontiguousarray(p.v[:, lo:hi]),
+                   p.cu_seqlens, (hi - lo) * G, hi - lo, p.d, p.causal, p.lam,
+                   cu_seqlens_k=p.cu_seqlens_k)

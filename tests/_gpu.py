@@ -16,7 +16,7 @@ import math
 import numpy as np
 import torch
 
-import _oracle_pool
+import _oracle_tile
 from oracle import layout, tile_walk
 
 MARGIN_TOL = 1e-3
@@ -111,11 +111,6 @@ def sample_items(p, max_items=None, seed=0, tail_heads=4):
     return sorted(pick)
 
 
-# Sampled tiles of a full-size layer visit up to ~1000 key tiles each: past
-# this many tile visits in one comparison, the oracle runs on a process pool.
-POOL_VISITS = 20000
-
-
 def compare(p, g, items=None, fp8=None, check_bits=True):
     """Compare a GPU result with the oracle on ``items`` (all query tiles by
     default); return a dict of metrics, asserting the tolerances. The count
@@ -136,13 +131,8 @@ def compare(p, g, items=None, fp8=None, check_bits=True):
         assert not row[last + 1:].any(), f"bit set on an unvisited tile of {item}"
         gots.append(row[:last + 1])
         visits += last + 1
-    if visits > POOL_VISITS:
-        key = (p.name, p.total_tokens, id(arrays[0]), fp8 is not None)
-        refs = _oracle_pool.pool_references(key, arrays, scales, cu, cuk, p.Hq, p.Hkv, causal, lam,
-                                            items, gots)
-    else:
-        refs = [_oracle_pool.reference(arrays, scales, cu, cuk, p.Hq, p.Hkv, causal, lam, it, got)
-                for it, got in zip(items, gots)]
+    refs = [_oracle_tile.reference(arrays, scales, cu, cuk, p.Hq, p.Hkv, causal, lam, it, got)
+            for it, got in zip(items, gots)]
     bad_bits = near = 0
     o_max = o_sum = 0.0
     o_cnt = 0
