@@ -322,9 +322,8 @@ bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
   Workspace *ws = nullptr;
   if ((st = scratch_for(ss, stream, sizeof(Workspace), &ws)) != BSA_OK) return st;
   const int rows = group * max_seqlen_q;
-  // 16-tile splits unless that leaves fewer than four work items per SM
-  const int split = (int64_t)Hkv * (total_k / bsa::kTile) / 16 < 4LL * info->sm_count ? 8 : 16;
-  const bsa::DecLayout layout = bsa::DecLayout::make(n_seqs, Hq, Hkv, rows, total_k, split);
+  const int split = bsa::decode_split(rows);
+  const bsa::DecLayout layout = bsa::DecLayout::make(n_seqs, Hkv, rows, total_k, split);
   void *buf = nullptr;
   if ((st = table_for(ss->dec, stream, layout.bytes, &buf)) != BSA_OK) return st;
   char *base = static_cast<char *>(buf);
@@ -334,12 +333,12 @@ bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
   p.q = q;
   p.cu_q = cu_seqlens_q;
   p.cu_k = cu_seqlens_k;
-  p.tile_off = reinterpret_cast<const int64_t *>(base + layout.tile_off);
   p.item_off = reinterpret_cast<const int32_t *>(base + layout.item_off);
   p.bm_off = reinterpret_cast<const int64_t *>(base + layout.bm_off);
-  p.S = reinterpret_cast<float *>(base + layout.S);
-  p.rm = reinterpret_cast<float *>(base + layout.rm);
-  p.smax = reinterpret_cast<float *>(base + layout.smax);
+  p.flags = reinterpret_cast<uint32_t *>(base + layout.flags);
+  p.done = reinterpret_cast<int32_t *>(base + layout.done);
+  p.agg = reinterpret_cast<float *>(base + layout.agg);
+  p.incl = reinterpret_cast<float *>(base + layout.incl);
   p.pO = reinterpret_cast<float *>(base + layout.pO);
   p.pm = reinterpret_cast<float *>(base + layout.pm);
   p.pl = reinterpret_cast<float *>(base + layout.pl);
@@ -347,13 +346,13 @@ bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
   p.lse = lse;
   p.bitmap = skip_bitmap;
   p.total_k = total_k;
-  p.max_tiles = layout.max_tiles;
-  p.max_splits = layout.max_items / Hkv;
+  p.max_items = layout.max_items;
   p.n_seqs = n_seqs;
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.group = group;
   p.rows = rows;
+  p.mpitch = (rows + 3) / 4 * 4;
   p.max_q = max_seqlen_q;
   p.split = split;
   p.causal = causal;

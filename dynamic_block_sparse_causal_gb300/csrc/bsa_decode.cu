@@ -10,21 +10,35 @@
 // Splitting the key range needs the order rule restated. A skipped tile never
 // raises the running max (tile_max < m + ln(lambda) < m for lambda < 1), so the
 // running max before tile j is the prefix max of the tile maxima before j, and
-// every decision depends on the tile maxima alone. The path therefore:
-//  1. dec_scores_kernel: for every (sequence, KV head, 16-tile split), the
-//     scaled scores S (log2 units) of the group's query rows against each key
-//     tile (TMA-staged, 3-stage ring) and their per-tile row maxima;
-//  2. dec_pv_kernel: per split, the decisions (the prefix max of the earlier
-//     tiles' maxima, then the split's tiles in order; the AND over each query
-//     head's rows), the kept tiles' V (TMA, only kept tiles) and an online
-//     softmax with the split's own reference max;
-//  3. dec_combine_kernel: merges the splits' (max, sum, output) per row.
-// The decisions are exactly those of the sequential walk; outputs equal the
-// online softmax over the kept tiles up to rounding order. The work is
-// bound by reading K once and the kept V once from DRAM; the two narrow
-// contractions (scores, P V) run on the tensor cores because the CUDA-core
-// versions were bound by shared-memory traffic, not by DRAM. One query row
-// group of at most 32 rows per KV head.
+// every decision depends on the tile maxima alone.
+//
+// One persistent kernel, one CTA per SM, takes work items (sequence, KV head,
+// split of 8 or 4 key tiles) from an atomic counter in index order. Per item:
+//   scores   S^T = K Q^T on the tensor cores for the split's tiles (K streamed
+//            by TMA through a 4-stage ring), kept in TMEM (three items' worth,
+//            so that P V work of a split does not hold up the K stream); their
+//            per-tile row maxima go to shared memory and the split's row
+//            maxima are published;
+//   decide   the prefix max before the split, from the published maxima of
+//            the earlier splits of the same (sequence, KV head) (a look-back
+//            that stops at the nearest split that has published its inclusive
+//            prefix), then the split's tiles in order, per query row; the AND
+//            over each query head's rows gives its skip bits;
+//   P V      for the kept tiles only: V by TMA (all of them prefetched into
+//            L2 once the decisions are out), P from the S still in TMEM,
+//            O^T = V^T P^T on the tensor cores, an online softmax with the
+//            split's own reference max;
+//   merge    the item of a (sequence, KV head) that finishes last (a counter)
+//            merges the partial results of the splits that kept a tile; no
+//            item waits for that.
+// Published maxima need no fences: the prologue fills them with NaN, a
+// writer stores the value (never NaN) with one relaxed 32-bit store, and a
+// reader polls until it reads a number. An item waits only for items of lower
+// index; those were claimed earlier by CTAs that are running and publish
+// their maxima before they wait for anything outside their CTA, so the waits
+// end; each is bounded by the wait limit all the same. Decisions equal the sequential walk's; outputs equal
+// the online softmax over the kept tiles up to rounding order. The work is
+// bound by reading K once and the kept V once from DRAM.
 #include <cuda_bf16.h>
 
 #include <climits>
@@ -39,11 +53,12 @@ namespace {
 
 constexpr uint32_t kTileBytes = 32768;   // 128 keys x 128 bf16
 constexpr uint32_t kBoxBytes = 16384;    // one 128-row x 128-byte TMA box
-constexpr int kStages = 3;
 constexpr float kLn2 = 0.6931471805599453f;
 
+constexpr uint32_t kFlagPart = 1;   // a work item's partial output is written (it kept a tile)
+
 struct DecItem {
-  int s, kvh, j0, j1, aq, Lq, ak, Lk;
+  int s, kvh, q, j0, j1, aq, Lq, ak, Lk, ns;
 };
 
 __device__ __forceinline__ void decode_item(const DecParams &p, int item, DecItem &it) {
@@ -58,12 +73,13 @@ __device__ __forceinline__ void decode_item(const DecParams &p, int item, DecIte
   it.ak = p.cu_k[lo];
   it.Lk = p.cu_k[lo + 1] - it.ak;
   const int nk = (it.Lk + kTile - 1) / kTile;
+  it.ns = (nk + p.split - 1) / p.split;
   // the KV heads of one split are neighbours: CTAs running together read
   // whole token rows of K and V (all heads) from DRAM
   const int local = item - p.item_off[lo];
-  const int split = local / p.Hkv;
-  it.kvh = local - split * p.Hkv;
-  it.j0 = split * p.split;
+  it.q = local / p.Hkv;
+  it.kvh = local - it.q * p.Hkv;
+  it.j0 = it.q * p.split;
   it.j1 = min(nk, it.j0 + p.split);
 }
 
@@ -74,15 +90,91 @@ __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, 
   tma_load_3d(dst + kBoxBytes, map, bar, 64, head, row);
 }
 
-// Plain bulk copy global -> shared, completing on an mbarrier (16-byte
-// aligned addresses, size a multiple of 16).
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
+// Four published maxima at once (16-byte aligned); several can be in flight.
+__device__ __forceinline__ float4 ld_volatile4(const float *a) {
+  float4 v;
+  asm volatile("ld.volatile.global.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(a));
+  return v;
 }
+__device__ __forceinline__ void st_relaxed(float *a, float v) {
+  asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(a), "f"(v) : "memory");
+}
+__device__ __forceinline__ int atom_add_acq_rel(int32_t *a, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
+  return old;
+}
+
+// Wait for a phase of an mbarrier; false when the CTA is aborting or the wait
+// ran past the limit (then the CTA aborts).
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, uint64_t limit,
+                                         volatile int *abort) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(a, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+// The first R of RB published maxima at a (16-byte aligned, RB a multiple
+// of 4) into v, loads in flight together.
+template <int RB>
+__device__ __forceinline__ void load_maxima(const float *a, int R, float (&v)[RB]) {
+#pragma unroll
+  for (int r = 0; r < RB; r += 4) {
+    float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    if (r < R) x = ld_volatile4(a + r);
+    v[r] = x.x;
+    v[r + 1] = x.y;
+    v[r + 2] = x.z;
+    v[r + 3] = x.w;
+  }
+}
+template <int RB>
+__device__ __forceinline__ bool all_published(const float (&v)[RB], int R) {
+  bool ok = true;
+#pragma unroll
+  for (int r = 0; r < RB; ++r) ok = ok && (r >= R || !isnan(v[r]));
+  return ok;
+}
+
+// Wait until another CTA has published the first R maxima at a (slots hold
+// NaN until then); false on a CTA or grid abort, or past the limit.
+template <int RB>
+__device__ __forceinline__ bool wait_maxima(const float *a, int R, float (&v)[RB], uint64_t limit,
+                                            volatile int *abort, const volatile int32_t *gabort) {
+  load_maxima<RB>(a, R, v);
+  if (all_published<RB>(v, R)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(64);
+    load_maxima<RB>(a, R, v);
+    if (all_published<RB>(v, R)) return true;
+    if (*abort || *gabort) return false;
+    if (globaltimer_ns() - t0 > limit) return false;
+  }
+}
+
+// Maximum over the warp in one redux: floats map to int32 keys that compare
+// in the same order (negative floats have their magnitude bits flipped).
+__device__ __forceinline__ float warp_max(float x) {
+  const int i = __float_as_int(x);
+  const int k = __reduce_max_sync(0xffffffffu, i >= 0 ? i : i ^ 0x7FFFFFFF);
+  return __int_as_float(k >= 0 ? k : k ^ 0x7FFFFFFF);
+}
+
+// A published maximum is never NaN (NaN marks "not yet published").
+__device__ __forceinline__ float publishable(float m) { return isnan(m) ? -INFINITY : m; }
 
 }  // namespace
 
@@ -91,7 +183,8 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 __global__ void __launch_bounds__(1024) dec_prologue_kernel(const __grid_constant__ DecParams p) {
   __shared__ int s_bad;
   const int tid = threadIdx.x;
-  grid_dep_launch();   // the score kernel may set up meanwhile; it waits for this grid
+  grid_dep_launch();   // the decode kernel may set up meanwhile; it waits for this grid
+  grid_dep_wait();     // the previous kernel on the stream (possibly a decode) is done
   if (tid == 0)
     s_bad = p.cu_q[0] != 0 || p.cu_k[0] != 0 || (int64_t)p.cu_k[p.n_seqs] != p.total_k;
   __syncthreads();
@@ -103,36 +196,44 @@ __global__ void __launch_bounds__(1024) dec_prologue_kernel(const __grid_constan
   __syncthreads();
   if (tid == 0) {
     bool bad = s_bad != 0;
-    long long tiles = 0, items = 0, words = 0;
-    int64_t *tile_off = const_cast<int64_t *>(p.tile_off);
+    long long items = 0, words = 0;
     int64_t *bm_off = const_cast<int64_t *>(p.bm_off);
     int32_t *item_off = const_cast<int32_t *>(p.item_off);
     for (int s = 0; s < p.n_seqs && !bad; ++s) {
       const int Lq = p.cu_q[s + 1] - p.cu_q[s], Lk = p.cu_k[s + 1] - p.cu_k[s];
       const long long nk = (Lk + kTile - 1) / kTile, nq = (Lq + kTile - 1) / kTile;
-      tile_off[s] = tiles;
       item_off[s] = (int32_t)min(items, (long long)INT_MAX);
       bm_off[s] = words;
-      tiles += nk;
       if (Lq > 0) items += (long long)p.Hkv * ((nk + p.split - 1) / p.split);
       words += (long long)p.Hq * nq * ((nk + 31) / 32);
     }
-    tile_off[p.n_seqs] = tiles;
     item_off[p.n_seqs] = (int32_t)min(items, (long long)INT_MAX);
     bm_off[p.n_seqs] = words;
-    if (items > INT_MAX) bad = true;
+    if (items > p.max_items) bad = true;
     p.dw->total_items = bad ? 0 : (int32_t)items;
+    p.dw->next_item = 0;
+    p.dw->abort = 0;
     if (bad) atomicOr(&p.ws->status, kStatusBadSeqlens);
     s_bad = bad;
   }
   __syncthreads();
   if (s_bad) return;
-  // the split passes OR their skip bits into the bitmap
+  // the decode kernel ORs skip bits into the bitmap, counts finished items and
+  // publishes maxima into slots that hold NaN until then
   if (p.bitmap)
     for (int64_t w = tid; w < p.bm_off[p.n_seqs]; w += blockDim.x) p.bitmap[w] = 0u;
+  const int items = p.dw->total_items;
+  for (int x = tid; x < items; x += blockDim.x) p.flags[x] = 0u;
+  for (int x = tid; x < p.n_seqs * p.Hkv; x += blockDim.x) p.done[x] = 0;
+  for (int64_t x = tid; x < (int64_t)items * p.mpitch; x += blockDim.x) {
+    p.agg[x] = __int_as_float(0x7fc00000);
+    p.incl[x] = __int_as_float(0x7fc00000);
+  }
 }
 
-// ============================================================ 1: scores
+// ============================================================ decode
+
+namespace {
 
 // 32 lanes x 16 consecutive 32-bit TMEM columns; the wait is tied to the
 // destination registers.
@@ -153,506 +254,556 @@ __device__ __forceinline__ void tmem_wait_ld16(uint32_t (&v)[16]) {
 #undef BSA_R8
 #undef BSA_W8
 
-// S^T = K Q^T on the tensor cores: M = 128 keys, N = the group's query rows
-// padded to 16 or 32, K = head dim. The contraction is tiny (the pass is
-// bound by reading K from DRAM) but it takes the dot products off the CUDA
-// cores and out of shared memory, whose bandwidth bounded the FMA version.
-//   warps 0-3  epilogue: TMEM lane = key; scales, masks and stores S, row maxima
-//   warp 4     lane 0: TMA producer of the K ring (all items of this CTA)
-//   warp 5     TMEM allocation; lane 0 issues the MMAs
-// The query rows of an item are written by the epilogue warps into one of two
-// 128-byte-swizzled K-major buffers (the MMA's B operand).
+// N TMEM columns (N = 16 or 32) of this warp's 32 lanes into v.
 template <int N>
-__global__ void __launch_bounds__(kDecScoreThreads + 64, 2)
-dec_scores_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensorMap tk) {
+__device__ __forceinline__ void tmem_ldN(uint32_t taddr, uint32_t (&v)[N]) {
+  tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+  if constexpr (N > 16) tmem_ld16(taddr + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+  tmem_wait_ld16(*reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+  if constexpr (N > 16) tmem_wait_ld16(*reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+}
+
+// RB >= group x Lq query rows; N = RB rounded up to 16 is the MMA width; an
+// item's scores take 128 TMEM columns (kSplit tiles x N), three items' worth,
+// then two N-column P V accumulators.
+template <int RB>
+struct DecCfg {
+  static constexpr int N = RB < 16 ? 16 : RB;
+  static constexpr int kSplit = 128 / N;
+  static constexpr int KST = N == 16 ? 4 : 3;   // K ring stages
+  static constexpr int VST = 2;                 // V ring stages
+  static constexpr uint32_t kQBytes = N * 256;  // query rows, bf16, 128-byte swizzled
+  static constexpr uint32_t kPBytes = N * 256;  // P, bf16, 128-byte swizzled
+  static constexpr uint32_t kVOff = KST * kTileBytes;
+  static constexpr uint32_t kQOff = kVOff + VST * kTileBytes;
+  static constexpr uint32_t kPOff = kQOff + 2 * kQBytes;
+  static constexpr size_t kSmem = 1024 + kPOff + 2 * kPBytes;
+  static constexpr int kSBufs = 3;              // items whose scores TMEM holds
+  static constexpr uint32_t kDCol = kSBufs * 128;   // first P V accumulator column
+};
+
+constexpr int kGroup = 128;          // threads of the score group and of the P V group
+constexpr int kDecThreadsAll = 384;  // two groups + K producer, V producer, two MMA warps
+// Registers per thread: the launch gives every thread kRegsLaunch; the
+// producer / MMA warpgroup gives most of its share to the P V group.
+constexpr uint32_t kRegsLaunch = 168, kRegsIssue = 64, kRegsPV = 256;
+static_assert(kGroup * (kRegsLaunch + kRegsPV + kRegsIssue) <= kDecThreadsAll * kRegsLaunch,
+              "register split above the launch allocation");
+constexpr int kMaxSplitRB = 128;     // kSplit x RB: tile-max entries of one item
+
+}  // namespace
+
+// Roles:
+//   warps 0-3   score group: the scores of the split from TMEM (thread =
+//               key), per-tile row maxima, the split maxima published
+//   warps 4-7   P V group: look-back, decisions, skip bits, P of the kept
+//               tiles (thread = key), O (thread = head-dim column), partial
+//               results, the merge
+//   warp 8      claims items, stages their query rows (the score MMA's B
+//               operand); lane 0: TMA producer of the K ring
+//   warp 9      lane 0: TMA producer of the V ring (kept tiles only)
+//   warp 10     TMEM allocation; lane 0 issues the score MMAs
+//   warp 11     lane 0 issues the P V MMAs
+template <int RB>
+__global__ void __launch_bounds__(kDecThreadsAll, 1)
+dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensorMap tk,
+           const __grid_constant__ CUtensorMap tv) {
+  using C = DecCfg<RB>;
+  constexpr int N = C::N, KST = C::KST, VST = C::VST, SPL = C::kSplit;
+  // scores: bf16 x bf16 -> f32, both K-major, M = 128 keys, N rows
+  constexpr uint32_t kIdescS = IDesc<1, false, 128, N>::value;
+  // P V: A (V) MN-major (bit 15), B (P) K-major, M = 128 head-dim columns
+  constexpr uint32_t kIdescO = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) |
+                               ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
   extern __shared__ uint8_t smem_raw[];
-  __shared__ float red[2][kDecScoreThreads / 32][kDecMaxRows];
-  __shared__ uint64_t kfull[kStages], kempty[kStages], sfull[2], sempty[2], qready[2], qfree[2],
-      drain;
+  __shared__ float red[4][kMaxSplitRB];   // per warp: max over its 32 keys, [tile][row]
+  __shared__ float tmax[3][kMaxSplitRB];  // per score buffer: tile row maxima, [tile][row]
+  __shared__ float mred[4][RB], lred[4][RB];
+  __shared__ int klist[2][SPL];
+  __shared__ uint32_t kact[2][SPL];
+  __shared__ int nkept_sh[2];
+  __shared__ int it_sh[4];
+  __shared__ int wmin[4], wcnt[4], clist[kGroup];
+  __shared__ int merge_sh;
+  __shared__ float pmsh[16][RB], plsh[16][RB], wsh[16][RB];
+  __shared__ float msh[RB], lsh[RB], scsh[RB];
+  __shared__ uint64_t itfull[4], itempty[4], kfull[KST], kempty[KST], vfull[VST], vempty[VST],
+      qready[2], qfree[2], sfull[3], sfree[3], mready[3], lready[2], lfree[2], pready[2], pfree[2],
+      dfull[2], dempty[2], drain[2];
   __shared__ uint32_t tmem_sh;
   __shared__ volatile int abort_sh;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
-  uint8_t *ring = smem_raw + (sbase - raw);
-  uint8_t *qbuf = ring + kStages * kTileBytes;   // two N x 256-byte buffers
-  constexpr uint32_t kQBytes = N * 256;
-  constexpr uint32_t kIdesc = IDesc<1, false, 128, N>::value;
-  constexpr int kEpi = kDecScoreThreads;
+  uint8_t *base = smem_raw + (sbase - raw);
   if (t == 0) {
-    for (int b = 0; b < kStages; ++b) {
+    for (int b = 0; b < 4; ++b) {
+      mbar_init(&itfull[b], 1);
+      mbar_init(&itempty[b], 5);   // score MMA, score group, P V group, V producer, P V MMA
+    }
+    for (int b = 0; b < KST; ++b) {
       mbar_init(&kfull[b], 1);
       mbar_init(&kempty[b], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < VST; ++b) {
+      mbar_init(&vfull[b], 1);
+      mbar_init(&vempty[b], 1);
+    }
+    for (int b = 0; b < 3; ++b) {
       mbar_init(&sfull[b], 1);
-      mbar_init(&sempty[b], kEpi / 32);
+      mbar_init(&sfree[b], 1);
+      mbar_init(&mready[b], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&qready[b], 1);
       mbar_init(&qfree[b], 1);
-    }
-    mbar_init(&drain, 1);
-    fence_mbar_init();
-    abort_sh = 0;
-  }
-  if (warp == 5) {
-    tmem_alloc(&tmem_sh, 2 * N < 32 ? 32 : 2 * N);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_sh;
-  grid_dep_wait();     // tables of the previous kernel
-  grid_dep_launch();
-  const int total = p.dw->total_items;
-  const uint64_t limit = p.wait_limit_ns;
-
-  if (warp == 4) {
-    // ---------------------------------------------------- TMA producer
-    if (lane == 0) {
-      uint32_t kc = 0;
-      int last_issue[kStages] = {-1, -1, -1};
-      bool ok = true;
-      for (int item = blockIdx.x; item < total && ok && !abort_sh; item += gridDim.x) {
-        DecItem it;
-        decode_item(p, item, it);
-        for (int j = it.j0; j < it.j1; ++j, ++kc) {
-          const uint32_t b = kc % kStages;
-          if (!(ok = mbar_wait(&kempty[b], ((kc / kStages) & 1) ^ 1, limit))) break;
-          if ((int)kc != p.debug_drop_k_load) {
-            load_tile(ring + b * kTileBytes, &tk, &kfull[b], it.kvh, it.ak + j * kTile);
-            last_issue[b] = (int)kc;
-          }
-        }
-      }
-      if (!ok) abort_sh = 1;
-      if (abort_sh)   // bounded wait for the copies still in flight
-        for (int b = 0; b < kStages; ++b)
-          if (last_issue[b] >= 0) mbar_wait(&kfull[b], (last_issue[b] / kStages) & 1, limit);
-    }
-  } else if (warp == 5) {
-    // ---------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      uint32_t kc = 0, sc = 0, i = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; item < total && ok && !abort_sh; item += gridDim.x, ++i) {
-        DecItem it;
-        decode_item(p, item, it);
-        const uint32_t par = i & 1;
-        if (!(ok = mbar_wait(&qready[par], (i >> 1) & 1, limit))) break;
-        const uint32_t qs = sbase + kStages * kTileBytes + par * kQBytes;
-        for (int j = it.j0; j < it.j1; ++j, ++kc, ++sc) {
-          const uint32_t b = kc % kStages, buf = sc & 1;
-          if (!(ok = mbar_wait(&kfull[b], (kc / kStages) & 1, limit))) break;
-          if (!(ok = mbar_wait(&sempty[buf], ((sc >> 1) & 1) ^ 1, limit))) break;
-          tc_fence_after();
-          const uint32_t ks = sbase + b * kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t ka = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            const uint32_t kb = (kk >> 2) * (N * 128) + (kk & 3) * 32;
-            mma_f16_ss(tmem + buf * N, sdesc_sw128(ks + ka, 16, 1024), sdesc_sw128(qs + kb, 16, 1024),
-                       kIdesc, kk > 0);
-          }
-          mma_commit(&sfull[buf]);
-          mma_commit(&kempty[b]);
-        }
-        if (!ok) break;
-        mma_commit(&qfree[par]);
-      }
-      if (!ok) abort_sh = 1;
-      if (abort_sh) {   // this thread's MMAs finish before TMEM is freed
-        mma_commit(&drain);
-        mbar_wait(&drain, 0, limit);
-      }
-    }
-  } else {
-    // ---------------------------------------------------- epilogue
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    uint32_t sc = 0, i = 0;
-    for (int item = blockIdx.x; item < total; item += gridDim.x, ++i) {
-      DecItem it;
-      decode_item(p, item, it);
-      const int R = p.group * it.Lq;
-      const uint32_t par = i & 1;
-      // B operand: query row r at 128-byte-swizzled K-major position
-      // control flow below follows barrier reductions only, so the four
-      // warps always agree (abort_sh is also written by the other roles)
-      bool ok = i < 2 || mbar_wait(&qfree[par], ((i >> 1) - 1) & 1, limit);
-      if (bar_red_or(!ok, 1, kEpi)) {
-        abort_sh = 1;
-        break;
-      }
-      bool stop = false;
-      uint8_t *qb = qbuf + par * kQBytes;
-      for (int c = t; c < N * 16; c += kEpi) {
-        const int r = c >> 4, ch = c & 15;
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (r < R) {
-          const int h = it.kvh * p.group + r / it.Lq, qi = r % it.Lq;
-          w = *reinterpret_cast<const uint4 *>(q + ((size_t)(it.aq + qi) * p.Hq + h) * kTile + ch * 8);
-        }
-        *reinterpret_cast<uint4 *>(qb + (ch >> 3) * (N * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = w;
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, kEpi);
-      if (t == 0) mbar_arrive(&qready[par]);
-      const int64_t toff = p.tile_off[it.s];
-      float split_max = -INFINITY;   // thread t < R: row t's max over this split
-      for (int j = it.j0; j < it.j1; ++j, ++sc) {
-        const uint32_t buf = sc & 1;
-        ok = mbar_wait(&sfull[buf], (sc >> 1) & 1, limit);
-        if (bar_red_or(!ok, 1, kEpi)) {
-          abort_sh = 1;
-          stop = true;
-          break;
-        }
-        tc_fence_after();
-        uint32_t v[N];
-        tmem_ld16(tmem + lane_off + buf * N, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-        if (N > 16) tmem_ld16(tmem + lane_off + buf * N + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[N > 16 ? 16 : 0]));
-        tmem_wait_ld16(*reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-        if (N > 16) tmem_wait_ld16(*reinterpret_cast<uint32_t(*)[16]>(&v[N > 16 ? 16 : 0]));
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sempty[buf]);
-        const int kpos = j * kTile + t;
-        const int64_t srow = ((toff + j) * p.Hkv + it.kvh) * p.rows;
-        const int u = j - it.j0;
-#pragma unroll
-        for (int r = 0; r < N; ++r) {
-          if (r < R) {
-            const int pos = it.Lk - it.Lq + r % it.Lq;   // this query's key position
-            const bool masked = kpos >= it.Lk || (p.causal && kpos > pos);
-            const float s2 = masked ? -INFINITY : __uint_as_float(v[r]) * p.c;
-            p.S[(srow + r) * kTile + t] = s2;
-            float m = s2;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if (lane == 0) red[u & 1][warp][r] = m;
-          }
-        }
-        named_bar_sync(1, kEpi);   // red[u & 1] complete
-        if (t < R) {
-          const float m = fmaxf(fmaxf(red[u & 1][0][t], red[u & 1][1][t]),
-                                fmaxf(red[u & 1][2][t], red[u & 1][3][t]));
-          p.rm[(it.kvh * p.max_tiles + toff + j) * p.rows + t] = m;
-          split_max = fmaxf(split_max, m);
-        }
-      }
-      if (stop) break;
-      // the split's row maxima, for the prefix max of the later splits
-      if (t < R)
-        p.smax[((int64_t)it.kvh * p.max_splits + p.item_off[it.s] / p.Hkv + it.j0 / p.split) *
-                   p.rows + t] = split_max;
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (abort_sh && t == 0) atomicOr(&p.ws->status, kStatusTimeout);
-  if (warp == 5) tmem_dealloc(tmem, 2 * N < 32 ? 32 : 2 * N);
-}
-
-// ============================================================ 2: decide, P V
-
-// One work item = (sequence, KV head, 16-tile split), as in the score pass.
-//   warps 0-3  decisions of the split: the row maxima of all earlier tiles
-//              (prefix max), then a walk over the split's tiles; skip bits go
-//              to the bitmap (OR into words the prologue zeroed). Then per
-//              kept tile: P (thread t = key t, fp32 exponentials and row sums)
-//              into a 128-byte-swizzled bf16 buffer, and O = alpha O + D
-//              (thread t = head-dim column t, D read from TMEM).
-//   warp 4     V producer for the kept tiles
-//   warp 5     TMEM allocation; lane 0 issues O^T = V^T P^T per kept tile:
-//              A = the V tile read MN-major (M = head dim), B = P (the
-//              group's rows padded to N, keys contiguous), D in one of two
-//              TMEM buffers.
-// RB >= group x Lq rows; N = RB rounded up to 16.
-template <int RB>
-__global__ void __launch_bounds__(kDecScoreThreads + 64, RB <= 16 ? 2 : 1)
-dec_pv_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensorMap tv) {
-  constexpr int N = RB < 16 ? 16 : RB;
-  constexpr int kEpi = kDecScoreThreads;
-  constexpr uint32_t kPBytes = N * 256;
-  // ring stage: the V tile, then the kept tile's scores S (rows x 128 fp32)
-  constexpr uint32_t kStage = kTileBytes + RB * kTile * 4;
-  // bf16 x bf16 -> f32, A MN-major (bit 15), B K-major, M = 128, N
-  constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) |
-                              ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ float lred[kEpi / 32][RB];
-  __shared__ float mred[kEpi / 32][RB];
-  __shared__ float srm[kDecSplit * RB];
-  __shared__ uint32_t predmask[RB];
-  __shared__ uint64_t vfull[kStages], vempty[kStages], pready[2], pfree[2], dfull[2], dempty[2],
-      lready[2], lfree[2], drain;
-  __shared__ int klist[2][kDecSplit];
-  __shared__ uint32_t kact[2][kDecSplit];
-  __shared__ uint32_t act_sh[kDecSplit];
-  __shared__ int nkept_sh[2];
-  __shared__ uint32_t tmem_sh;
-  __shared__ volatile int abort_sh;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t sbase = (raw + 1023u) & ~1023u;
-  uint8_t *ring = smem_raw + (sbase - raw);
-  uint8_t *pbuf = ring + kStages * kStage;
-  if (t == 0) {
-    for (int b = 0; b < kStages; ++b) {
-      mbar_init(&vfull[b], 1);
-      mbar_init(&vempty[b], 2);   // the MMA has read V, the epilogue has read S
-    }
-    for (int b = 0; b < 2; ++b) {
+      mbar_init(&lready[b], 1);
+      mbar_init(&lfree[b], 2);   // V producer, P V MMA
       mbar_init(&pready[b], 1);
       mbar_init(&pfree[b], 1);
       mbar_init(&dfull[b], 1);
-      mbar_init(&dempty[b], kEpi / 32);
-      mbar_init(&lready[b], 1);
-      mbar_init(&lfree[b], 2);
+      mbar_init(&dempty[b], kGroup / 32);
+      mbar_init(&drain[b], 1);
     }
-    mbar_init(&drain, 1);
     fence_mbar_init();
     abort_sh = 0;
   }
-  if (warp == 5) {
-    tmem_alloc(&tmem_sh, 2 * N < 32 ? 32 : 2 * N);
+  if (warp == 10) {
+    tmem_alloc(&tmem_sh, 512);
     tmem_relinquish();
   }
+  // the P buffers start zeroed: rows past RB are never written again
+  for (uint32_t x = t; x < 2 * C::kPBytes / 16; x += kDecThreadsAll)
+    reinterpret_cast<uint4 *>(base + C::kPOff)[x] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_sh;
-  grid_dep_wait();     // tables of the previous kernel
+  grid_dep_wait();     // tables of the prologue
   grid_dep_launch();
   const int total = p.dw->total_items;
   const uint64_t limit = p.wait_limit_ns;
+  const volatile int32_t *gabort = &p.dw->abort;
 
-  if (warp == 4) {
-    // ---------------------------------------------------- V producer
-    if (lane == 0) {
-      uint32_t kc = 0, i = 0;
-      int last_issue[kStages] = {-1, -1, -1};
-      bool ok = true;
-      for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++i) {
+  if (warp >= 8) {
+    reg_dealloc<kRegsIssue>();
+    if (warp == 8) {
+      // ---------------------------------------------------- claims, Q rows, K producer
+      const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
+      uint32_t kc = 0;
+      int last_issue[KST];
+  #pragma unroll
+      for (int b = 0; b < KST; ++b) last_issue[b] = -1;
+      for (uint32_t i = 0;; ++i) {
+        const uint32_t slot = i & 3, par = i & 1;
+        int item = -1;
+        bool ok = true;
+        if (lane == 0) {
+          ok = wait_bar(&itempty[slot], ((i >> 2) & 1) ^ 1, limit, &abort_sh);
+          if (ok && !abort_sh && !*gabort) {
+            item = atomicAdd(&p.dw->next_item, 1);
+            if (item >= total) item = -1;
+          }
+          if (ok) {
+            it_sh[slot] = item;
+            mbar_arrive(&itfull[slot]);
+          }
+          // the score MMAs of the item two back have read this query buffer
+          if (ok && item >= 0 && i >= 2) ok = wait_bar(&qfree[par], ((i >> 1) - 1) & 1, limit, &abort_sh);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if (!ok || item < 0) break;
         DecItem it;
         decode_item(p, item, it);
-        const uint32_t par = i & 1;
-        if (!(ok = mbar_wait(&lready[par], (i >> 1) & 1, limit))) break;
-        const int n = nkept_sh[par];
+        // B operand: query row r at its 128-byte-swizzled K-major position
         const int R = p.group * it.Lq;
-        const int64_t toff = p.tile_off[it.s];
-        for (int u = 0; u < n; ++u) {
-          const uint32_t b = kc % kStages;
-          if (!(ok = mbar_wait(&vempty[b], ((kc / kStages) & 1) ^ 1, limit)) || abort_sh) {
-            ok = false;
-            break;
+        uint8_t *qb = base + C::kQOff + par * C::kQBytes;
+        for (int c = lane; c < N * 16; c += 32) {
+          const int r = c >> 4, ch = c & 15;
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
+          if (r < R) {
+            const int h = it.kvh * p.group + r / it.Lq, qi = r % it.Lq;
+            w = *reinterpret_cast<const uint4 *>(q + ((size_t)(it.aq + qi) * p.Hq + h) * kTile + ch * 8);
           }
-          const int j = klist[par][u];
-          uint8_t *st = ring + b * kStage;
-          mbar_expect_tx(&vfull[b], kTileBytes + R * kTile * 4);
-          tma_load_3d(st, &tv, &vfull[b], 0, it.kvh, it.ak + j * kTile);
-          tma_load_3d(st + kBoxBytes, &tv, &vfull[b], 64, it.kvh, it.ak + j * kTile);
-          bulk_load(st + kTileBytes, p.S + ((toff + j) * p.Hkv + it.kvh) * p.rows * kTile,
-                    R * kTile * 4, &vfull[b]);
-          last_issue[b] = (int)kc++;
+          *reinterpret_cast<uint4 *>(qb + (ch >> 3) * (N * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = w;
         }
-        mbar_arrive(&lfree[par]);
-      }
-      if (!ok) {
-        abort_sh = 1;
-        for (int b = 0; b < kStages; ++b)
-          if (last_issue[b] >= 0) mbar_wait(&vfull[b], (last_issue[b] / kStages) & 1, limit);
-      }
-    }
-  } else if (warp == 5) {
-    // ---------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      uint32_t kc = 0, i = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++i) {
-        const uint32_t par = i & 1;
-        if (!(ok = mbar_wait(&lready[par], (i >> 1) & 1, limit))) break;
-        const int n = nkept_sh[par];
-        mbar_arrive(&lfree[par]);
-        for (int u = 0; u < n; ++u, ++kc) {
-          const uint32_t b = kc % kStages, slot = kc & 1;
-          if (!(ok = mbar_wait(&vfull[b], (kc / kStages) & 1, limit))) break;
-          if (!(ok = mbar_wait(&pready[slot], (kc >> 1) & 1, limit))) break;
-          if (!(ok = mbar_wait(&dempty[slot], ((kc >> 1) & 1) ^ 1, limit))) break;
-          if (abort_sh) {
-            ok = false;
-            break;
+        fence_proxy_async_smem();
+        __syncwarp();
+        bool okk = true;
+        if (lane == 0) {
+          mbar_arrive(&qready[par]);
+          for (int j = it.j0; j < it.j1; ++j, ++kc) {
+            const uint32_t b = kc % KST;
+            if (!(okk = wait_bar(&kempty[b], ((kc / KST) & 1) ^ 1, limit, &abort_sh))) break;
+            if ((int)kc != p.debug_drop_k_load) {
+              load_tile(base + b * kTileBytes, &tk, &kfull[b], it.kvh, it.ak + j * kTile);
+              last_issue[b] = (int)kc;
+            }
           }
+        }
+        if (!__shfl_sync(0xffffffffu, okk, 0)) break;
+      }
+      if (lane == 0 && abort_sh)   // bounded wait for the copies still in flight
+        for (int b = 0; b < KST; ++b)
+          if (last_issue[b] >= 0) mbar_wait(&kfull[b], (last_issue[b] / KST) & 1, limit);
+    } else if (warp == 9) {
+      // ---------------------------------------------------- V producer
+      if (lane == 0) {
+        uint32_t vc = 0;
+        int last_issue[VST];
+  #pragma unroll
+        for (int b = 0; b < VST; ++b) last_issue[b] = -1;
+        for (uint32_t i = 0;; ++i) {
+          const uint32_t slot = i & 3, par = i & 1;
+          if (!wait_bar(&itfull[slot], (i >> 2) & 1, limit, &abort_sh)) break;
+          const int item = it_sh[slot];
+          mbar_arrive(&itempty[slot]);
+          if (item < 0) break;
+          DecItem it;
+          decode_item(p, item, it);
+          if (!wait_bar(&lready[par], (i >> 1) & 1, limit, &abort_sh)) break;
+          const int n = nkept_sh[par];
+          // every kept tile's V heads for L2 at once; the two ring stages then
+          // fill from L2 instead of waiting out DRAM latency tile by tile
+          for (int u = VST; u < n; ++u) {
+            tma_prefetch_3d(&tv, 0, it.kvh, it.ak + klist[par][u] * kTile);
+            tma_prefetch_3d(&tv, 64, it.kvh, it.ak + klist[par][u] * kTile);
+          }
+          bool ok = true;
+          for (int u = 0; u < n; ++u, ++vc) {
+            const uint32_t b = vc % VST;
+            if (!(ok = wait_bar(&vempty[b], ((vc / VST) & 1) ^ 1, limit, &abort_sh))) break;
+            load_tile(base + C::kVOff + b * kTileBytes, &tv, &vfull[b], it.kvh,
+                      it.ak + klist[par][u] * kTile);
+            last_issue[b] = (int)vc;
+          }
+          if (!ok) break;
+          mbar_arrive(&lfree[par]);
+        }
+        if (abort_sh)
+          for (int b = 0; b < VST; ++b)
+            if (last_issue[b] >= 0) mbar_wait(&vfull[b], (last_issue[b] / VST) & 1, limit);
+      }
+    } else if (warp == 10) {
+      // ---------------------------------------------------- score MMAs
+      if (lane == 0) {
+        uint32_t kc = 0;
+        for (uint32_t i = 0;; ++i) {
+          const uint32_t slot = i & 3, par = i & 1;
+          if (!wait_bar(&itfull[slot], (i >> 2) & 1, limit, &abort_sh)) break;
+          const int item = it_sh[slot];
+          mbar_arrive(&itempty[slot]);
+          if (item < 0) break;
+          DecItem it;
+          decode_item(p, item, it);
+          // the query rows are staged, and the P V group is done with the S
+          // columns of the item three back
+          const uint32_t sb = i % 3;
+          if (!wait_bar(&qready[par], (i >> 1) & 1, limit, &abort_sh)) break;
+          if (!wait_bar(&sfree[sb], ((i / 3) & 1) ^ 1, limit, &abort_sh)) break;
           tc_fence_after();
-          const uint32_t vs = sbase + b * kStage;
-          const uint32_t ps = sbase + kStages * kStage + slot * kPBytes;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            // A: 16 keys = two 8-key swizzle atoms (2048 bytes); the two 64-wide
-            // halves of the head dim are one box apart. B: 32 bytes per K step.
-            const uint64_t ad = sdesc_sw128(vs + kk * 2048, kBoxBytes, 1024);
-            const uint64_t bd = sdesc_sw128(ps + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
-            mma_f16_ss(tmem + slot * N, ad, bd, kIdesc, kk > 0);
+          const uint32_t qs = sbase + C::kQOff + par * C::kQBytes;
+          bool ok = true;
+          for (int j = it.j0; j < it.j1; ++j, ++kc) {
+            const uint32_t b = kc % KST;
+            if (!(ok = wait_bar(&kfull[b], (kc / KST) & 1, limit, &abort_sh))) break;
+            tc_fence_after();
+            const uint32_t ks = sbase + b * kTileBytes;
+            const uint32_t dcol = sb * 128 + (j - it.j0) * N;
+  #pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t ka = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+              const uint32_t kb = (kk >> 2) * (N * 128) + (kk & 3) * 32;
+              mma_f16_ss(tmem + dcol, sdesc_sw128(ks + ka, 16, 1024), sdesc_sw128(qs + kb, 16, 1024),
+                         kIdescS, kk > 0);
+            }
+            mma_commit(&kempty[b]);
           }
-          mma_commit(&dfull[slot]);
-          mma_commit(&vempty[b]);
-          mma_commit(&pfree[slot]);
+          if (!ok) break;
+          mma_commit(&sfull[sb]);
+          mma_commit(&qfree[par]);
+        }
+        if (abort_sh) {   // this thread's MMAs finish before TMEM is freed
+          mma_commit(&drain[0]);
+          mbar_wait(&drain[0], 0, limit);
         }
       }
-      if (!ok) {
-        abort_sh = 1;
-        mma_commit(&drain);
-        mbar_wait(&drain, 0, limit);
+    } else {   // warp 11
+      // ---------------------------------------------------- P V MMAs
+      if (lane == 0) {
+        uint32_t vc = 0;
+        for (uint32_t i = 0;; ++i) {
+          const uint32_t slot = i & 3, par = i & 1;
+          if (!wait_bar(&itfull[slot], (i >> 2) & 1, limit, &abort_sh)) break;
+          const int item = it_sh[slot];
+          mbar_arrive(&itempty[slot]);
+          if (item < 0) break;
+          if (!wait_bar(&lready[par], (i >> 1) & 1, limit, &abort_sh)) break;
+          const int n = nkept_sh[par];
+          mbar_arrive(&lfree[par]);
+          bool ok = true;
+          for (int u = 0; u < n; ++u, ++vc) {
+            const uint32_t b = vc % VST, ps = vc & 1;
+            if (!(ok = wait_bar(&vfull[b], (vc / VST) & 1, limit, &abort_sh))) break;
+            if (!(ok = wait_bar(&pready[ps], (vc >> 1) & 1, limit, &abort_sh))) break;
+            if (!(ok = wait_bar(&dempty[ps], ((vc >> 1) & 1) ^ 1, limit, &abort_sh))) break;
+            tc_fence_after();
+            const uint32_t vs = sbase + C::kVOff + b * kTileBytes;
+            const uint32_t pb = sbase + C::kPOff + ps * C::kPBytes;
+  #pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              // A: 16 keys = two 8-key swizzle atoms (2048 bytes); the two 64-wide
+              // halves of the head dim are one box apart. B: 32 bytes per K step.
+              const uint64_t ad = sdesc_sw128(vs + kk * 2048, kBoxBytes, 1024);
+              const uint64_t bd = sdesc_sw128(pb + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
+              mma_f16_ss(tmem + C::kDCol + ps * N, ad, bd, kIdescO, kk > 0);
+            }
+            mma_commit(&dfull[ps]);
+            mma_commit(&vempty[b]);
+            mma_commit(&pfree[ps]);
+          }
+          if (!ok) break;
+        }
+        if (abort_sh) {
+          mma_commit(&drain[1]);
+          mbar_wait(&drain[1], 0, limit);
+        }
       }
     }
-  } else {
-    // ---------------------------------------------------- epilogue
+  } else if (warp < 4) {
+    // ---------------------------------------------------- score group
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    uint32_t kc = 0, i = 0;
-    bool stop = false;
-    for (int item = blockIdx.x; item < total && !stop; item += gridDim.x, ++i) {
+    for (uint32_t i = 0;; ++i) {
+      const uint32_t slot = i & 3, sb = i % 3;
+      // control flow follows barrier reductions only, so the four warps agree
+      bool ok = wait_bar(&itfull[slot], (i >> 2) & 1, limit, &abort_sh);
+      const int item = ok ? it_sh[slot] : -1;
+      if (bar_red_or(!ok, 1, kGroup)) break;
+      if (t == 0) mbar_arrive(&itempty[slot]);
+      if (item < 0) break;
       DecItem it;
       decode_item(p, item, it);
       const int R = p.group * it.Lq, nt = it.j1 - it.j0;
-      const int64_t toff = p.tile_off[it.s];
-      const uint32_t par = i & 1;
-      const float *rmh = p.rm + ((int64_t)it.kvh * p.max_tiles + toff) * p.rows;
-      // ---- decisions. Running max before the split: the max of the earlier
-      // splits' row maxima (written by the score pass). Rp (R rounded up to a
-      // power of two) divides the thread stride, so thread t always meets row
-      // t % Rp; the split's own tile maxima go to shared memory for the walk
-      // in order.
-      const int Rp = R <= 1 ? 1 : 1 << (32 - __clz(R - 1));
-      const int rt = t & (Rp - 1);
-      float mp = -INFINITY;
-      if (rt < R) {
-        const float *sm = p.smax + ((int64_t)it.kvh * p.max_splits + p.item_off[it.s] / p.Hkv) * p.rows;
-        const int q = it.j0 / p.split;   // splits before this one
-#pragma unroll 4
-        for (int idx = t; idx < q * Rp; idx += kEpi)
-          mp = fmaxf(mp, sm[(int64_t)(idx / Rp) * p.rows + rt]);
+      // key position of each row's query (rows past R: unused)
+      int pos[RB];
+#pragma unroll
+      for (int r = 0; r < RB; ++r) pos[r] = it.Lk - it.Lq + (r < R ? r % it.Lq : 0);
+      ok = wait_bar(&sfull[sb], (i / 3) & 1, limit, &abort_sh);
+      if (bar_red_or(!ok, 1, kGroup)) break;
+      tc_fence_after();
+      for (int u = 0; u < nt; ++u) {
+        uint32_t v[N];
+        tmem_ldN<N>(tmem + lane_off + sb * 128 + u * N, v);
+        const int kpos = (it.j0 + u) * kTile + t;
+        const bool out = kpos >= it.Lk;
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+          const bool masked = out || (p.causal && kpos > pos[r]);
+          const float m = warp_max(masked ? -INFINITY : __uint_as_float(v[r]) * p.c);
+          if (lane == 0) red[warp][u * RB + r] = m;
+        }
       }
-      for (int idx = t; idx < nt * R; idx += kEpi)
-        srm[idx] = rmh[(int64_t)(it.j0 + idx / R) * p.rows + idx % R];
-      for (int o = 16; o >= Rp; o >>= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
-      if (lane < Rp) mred[warp][lane] = mp;
-      // the lists of item i - 2 are no longer read by the producer and MMA
-      const bool okl = i < 2 || mbar_wait(&lfree[par], ((i >> 1) - 1) & 1, limit);
-      if (bar_red_or(!okl, 1, kEpi)) {
+      tc_fence_before();
+      named_bar_sync(1, kGroup);
+      for (int x = t; x < nt * RB; x += kGroup)
+        tmax[sb][x] = fmaxf(fmaxf(red[0][x], red[1][x]), fmaxf(red[2][x], red[3][x]));
+      if (t < R) {   // the split's row maxima, for the look-back of later splits
+        float m = -INFINITY;
+        for (int u = 0; u < nt; ++u)
+          m = fmaxf(m, fmaxf(fmaxf(red[0][u * RB + t], red[1][u * RB + t]),
+                             fmaxf(red[2][u * RB + t], red[3][u * RB + t])));
+        st_relaxed(p.agg + (int64_t)item * p.mpitch + t, publishable(m));
+      }
+      named_bar_sync(1, kGroup);
+      if (t == 0) mbar_arrive(&mready[sb]);
+    }
+    if (abort_sh && t == 0) atomicExch(const_cast<int32_t *>(gabort), 1);
+  } else {
+    reg_alloc<kRegsPV>();
+    // ---------------------------------------------------- P V group
+    const int tp = t - kGroup, wp = warp - 4;   // key, head-dim column; warp in group
+    const uint32_t lane_off = (uint32_t)(wp * 32) << 16;
+    uint32_t kc = 0;
+    bool stop = false;
+    for (uint32_t i = 0; !stop; ++i) {
+      const uint32_t slot = i & 3, par = i & 1, sb = i % 3;
+      bool ok = wait_bar(&itfull[slot], (i >> 2) & 1, limit, &abort_sh);
+      const int item = ok ? it_sh[slot] : -1;
+      if (bar_red_or(!ok, 2, kGroup)) break;
+      if (tp == 0) mbar_arrive(&itempty[slot]);
+      if (item < 0) break;
+      DecItem it;
+      decode_item(p, item, it);
+      const int R = p.group * it.Lq, nt = it.j1 - it.j0;
+      const int64_t first = (int64_t)p.item_off[it.s] + it.kvh;   // split qq is first + qq * Hkv
+      const int64_t bmo = p.bitmap ? p.bm_off[it.s] : 0;
+
+      // ---- running max before the split (while the score group still works
+      // on this split): nearest earlier splits first, 128 at a time, down to
+      // the nearest one with an inclusive prefix
+      float mp[RB];
+#pragma unroll
+      for (int r = 0; r < RB; ++r) mp[r] = -INFINITY;
+      bool fail = false, anyfail = false;
+      for (int hi = it.q; hi > 0; hi -= kGroup) {
+        // thread tp: split qq; its row maxima (waited for) and, if every
+        // row's inclusive prefix is out already, those
+        const int qq = hi - 1 - tp;
+        const bool mine = tp < hi;   // qq >= 0; the window is hi-128 .. hi-1
+        const int64_t prow = (first + (int64_t)qq * p.Hkv) * p.mpitch;
+        float a[RB], c[RB];
+        bool incl_ok = false;
+        if (mine) {
+          load_maxima<RB>(p.incl + prow, R, c);
+          incl_ok = all_published<RB>(c, R);
+          if (!wait_maxima<RB>(p.agg + prow, R, a, limit, &abort_sh, gabort)) fail = true;
+        }
+        if (bar_red_or(fail, 2, kGroup)) {
+          anyfail = true;
+          break;
+        }
+        const unsigned bal = __ballot_sync(0xffffffffu, incl_ok);
+        if (lane == 0) wmin[wp] = bal ? wp * 32 + __ffs(bal) - 1 : INT_MAX;
+        named_bar_sync(2, kGroup);
+        const int tmin = min(min(wmin[0], wmin[1]), min(wmin[2], wmin[3]));
+        if (mine && tp <= tmin) {
+#pragma unroll
+          for (int r = 0; r < RB; ++r)
+            if (r < R) mp[r] = fmaxf(mp[r], tp == tmin ? c[r] : a[r]);
+        }
+        named_bar_sync(2, kGroup);   // wmin is rewritten by the next window
+        if (tmin != INT_MAX) break;
+      }
+      if (anyfail) {
         stop = true;
         break;
       }
-      if (t < R) {   // walk the split's tiles in order, per row
-        float mr = fmaxf(fmaxf(mred[0][t], mred[1][t]), fmaxf(mred[2][t], mred[3][t]));
-        uint32_t bits = 0;   // bit u: row t would skip tile j0 + u
-        for (int u = 0; u < nt; ++u) {
-          const float x = srm[u * R + t];
-          if (x < mr + p.log2_lambda) bits |= 1u << u;
-          mr = fmaxf(mr, x);
-        }
-        predmask[t] = bits;
+#pragma unroll
+      for (int r = 0; r < RB; ++r) {
+        const float m = warp_max(mp[r]);
+        if (lane == 0) mred[wp][r] = m;
       }
-      named_bar_sync(1, kEpi);
-      if (t < nt) {   // heads of the group that keep tile j0 + t
-        uint32_t act = 0;
-        for (int g = 0; g < p.group; ++g) {
-          bool keep = false;
-          for (int qi = 0; qi < it.Lq; ++qi) keep |= !((predmask[g * it.Lq + qi] >> t) & 1u);
-          if (keep) act |= 1u << g;
+      // this split's tile maxima are in, and the kept lists of the item two
+      // back are no longer read
+      ok = wait_bar(&mready[sb], (i / 3) & 1, limit, &abort_sh) &&
+           wait_bar(&lfree[par], ((i >> 1) & 1) ^ 1, limit, &abort_sh);
+      if (bar_red_or(!ok, 2, kGroup)) break;
+      tc_fence_after();
+
+      // ---- decisions, in the group's first warp (R <= 32 rows): walk the
+      // split's tiles in order per row; a head skips a tile when all its rows
+      // do; the kept list and the skip bits follow from ballots
+      if (wp == 0) {
+        uint32_t bits = 0;   // bit u: row lane would skip tile j0 + u
+        if (lane < R) {
+          float mr = fmaxf(fmaxf(mred[0][lane], mred[1][lane]), fmaxf(mred[2][lane], mred[3][lane]));
+          for (int u = 0; u < nt; ++u) {
+            const float x = tmax[sb][u * RB + lane];
+            if (x < mr + p.log2_lambda) bits |= 1u << u;
+            mr = fmaxf(mr, x);
+          }
+          // max over every tile up to the split's end: the later splits' look-back
+          st_relaxed(p.incl + (int64_t)item * p.mpitch + lane, publishable(mr));
         }
-        act_sh[t] = act;
-      }
-      named_bar_sync(1, kEpi);
-      if (t == 0) {
+        // lane g < group: the tiles head g skips (the AND over its query rows)
+        uint32_t hs = nt >= 32 ? 0xFFFFFFFFu : ((1u << nt) - 1u);
+        for (int qi = 0; qi < it.Lq; ++qi) {
+          const uint32_t b = __shfl_sync(0xffffffffu, bits, (lane * it.Lq + qi) & 31);
+          hs &= b;
+        }
+        const bool head = lane < p.group;
         int n = 0;
-        for (int u = 0; u < nt; ++u)
-          if (act_sh[u]) {
-            klist[par][n] = it.j0 + u;
-            kact[par][n] = act_sh[u];
+        for (int u = 0; u < nt; ++u) {
+          const uint32_t act = __ballot_sync(0xffffffffu, head && !((hs >> u) & 1u));
+          if (act) {
+            if (lane == 0) {
+              klist[par][n] = it.j0 + u;
+              kact[par][n] = act;
+            }
             ++n;
           }
-        nkept_sh[par] = n;
-        mbar_arrive(&lready[par]);
+        }
+        if (lane == 0) {
+          nkept_sh[par] = n;
+          mbar_arrive(&lready[par]);
+        }
+        if (p.bitmap && head && hs) {   // this split's bits of each head's row
+          const int nk = (it.Lk + kTile - 1) / kTile, W = (nk + 31) / 32;
+          atomicOr(p.bitmap + bmo + (int64_t)(it.kvh * p.group + lane) * W + (it.j0 >> 5),
+                   hs << (it.j0 & 31));
+        }
       }
-      if (p.bitmap && t < p.group) {   // this split's 16 bits of each head's row
-        uint32_t bits = 0xFFFFu;
-        for (int qi = 0; qi < it.Lq; ++qi) bits &= predmask[t * it.Lq + qi];
-        bits &= (nt >= 32 ? 0xFFFFFFFFu : ((1u << nt) - 1u));
-        const int nk = (it.Lk + kTile - 1) / kTile, W = (nk + 31) / 32;
-        if (bits)
-          atomicOr(p.bitmap + p.bm_off[it.s] + (int64_t)(it.kvh * p.group + t) * W + (it.j0 >> 5),
-                   bits << (it.j0 & 31));
-      }
-      named_bar_sync(1, kEpi);
+      named_bar_sync(2, kGroup);
       const int n = nkept_sh[par];
+
       // ---- kept tiles
       float O[RB], mref[RB], lsum[RB], alpha[RB], alpha_prev[RB];
+      int hrow[RB], posr[RB];   // head (in the group) and query key position of each row
 #pragma unroll
       for (int r = 0; r < RB; ++r) {
         O[r] = 0.f;
         mref[r] = -INFINITY;
         lsum[r] = 0.f;
         alpha[r] = alpha_prev[r] = 1.f;
+        hrow[r] = r < R ? r / it.Lq : 31;
+        posr[r] = it.Lk - it.Lq + (r < R ? r % it.Lq : 0);
       }
-      // O += D of kept tile number kd (its P used the reference alpha_prev)
+      // O = alpha_prev O + D of kept tile number kd
       auto take_d = [&](uint32_t kd) -> bool {
-        const uint32_t slot = kd & 1;
-        const bool okd = mbar_wait(&dfull[slot], (kd >> 1) & 1, limit);
-        if (bar_red_or(!okd, 1, kEpi)) return false;
+        const uint32_t ps = kd & 1;
+        const bool okd = wait_bar(&dfull[ps], (kd >> 1) & 1, limit, &abort_sh);
+        if (bar_red_or(!okd, 2, kGroup)) return false;
         tc_fence_after();
         uint32_t v[N];
-#pragma unroll
-        for (int h = 0; h < N / 16; ++h)
-          tmem_ld16(tmem + lane_off + slot * N + h * 16, *reinterpret_cast<uint32_t(*)[16]>(&v[h * 16]));
-#pragma unroll
-        for (int h = 0; h < N / 16; ++h) tmem_wait_ld16(*reinterpret_cast<uint32_t(*)[16]>(&v[h * 16]));
+        tmem_ldN<N>(tmem + lane_off + C::kDCol + ps * N, v);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&dempty[slot]);
+        if (lane == 0) mbar_arrive(&dempty[ps]);
 #pragma unroll
         for (int r = 0; r < RB; ++r) O[r] = fmaf(O[r], alpha_prev[r], __uint_as_float(v[r]));
         return true;
       };
       for (int u = 0; u < n && !stop; ++u, ++kc) {
         const int j = klist[par][u];
-        const uint32_t act = kact[par][u], slot = kc & 1, b = kc % kStages;
-        const float *rmj = rmh + (int64_t)j * p.rows;
-        // P buffer slot free (the MMA two kept tiles back has read it), and
-        // this tile's V and S landed
-        const bool okp = mbar_wait(&pfree[slot], ((kc >> 1) & 1) ^ 1, limit) &&
-                         mbar_wait(&vfull[b], (kc / kStages) & 1, limit);
-        if (bar_red_or(!okp, 1, kEpi)) {
+        const uint32_t act = kact[par][u], ps = kc & 1;
+        const float *tm = tmax[sb] + (j - it.j0) * RB;
+        // P buffer free: the MMA two kept tiles back has read it
+        ok = wait_bar(&pfree[ps], ((kc >> 1) & 1) ^ 1, limit, &abort_sh);
+        if (bar_red_or(!ok, 2, kGroup)) {
           stop = true;
           break;
         }
-        const float *Ss = reinterpret_cast<const float *>(ring + b * kStage + kTileBytes);
-        uint8_t *pb = pbuf + slot * kPBytes;
+        uint32_t v[N];
+        tmem_ldN<N>(tmem + lane_off + sb * 128 + (j - it.j0) * N, v);
+        const int kpos = j * kTile + tp;
+        const bool outside = kpos >= it.Lk;
+        uint8_t *pb = base + C::kPOff + ps * C::kPBytes;
+        // rows past RB stay zero from the start of the kernel
 #pragma unroll
-        for (int r = 0; r < N; ++r) {
+        for (int r = 0; r < RB; ++r) {
           float pv = 0.f;
-          if (r < RB && r < R) {
-            const bool on = (act >> (r / it.Lq)) & 1u;
-            const float mnew = on ? fmaxf(mref[r], rmj[r]) : mref[r];
+          if (r < R) {
+            const bool on = (act >> hrow[r]) & 1u;
+            const float mnew = on ? fmaxf(mref[r], tm[r]) : mref[r];
             alpha[r] = mnew == -INFINITY ? 1.f : ex2_approx(mref[r] - mnew);
             mref[r] = mnew;
-            pv = (on && mnew != -INFINITY) ? ex2_approx(Ss[r * kTile + t] - mnew) : 0.f;
+            const bool masked = outside || (p.causal && kpos > posr[r]);
+            const float s2 = masked ? -INFINITY : __uint_as_float(v[r]) * p.c;
+            pv = (on && mnew != -INFINITY) ? ex2_approx(s2 - mnew) : 0.f;
             lsum[r] = fmaf(lsum[r], alpha[r], pv);
-          } else if (r < RB) {
+          } else {
             alpha[r] = 1.f;
           }
-          // key t of row r: box t/64, 16-byte chunk (t%64)/8 swizzled by row
-          *reinterpret_cast<__nv_bfloat16 *>(pb + (t >> 6) * (N * 128) + r * 128 +
-                                             ((((t >> 3) & 7) ^ (r & 7)) << 4) + (t & 7) * 2) =
+          // key tp of row r: box tp/64, 16-byte chunk (tp%64)/8 swizzled by row
+          *reinterpret_cast<__nv_bfloat16 *>(pb + (tp >> 6) * (N * 128) + r * 128 +
+                                             ((((tp >> 3) & 7) ^ (r & 7)) << 4) + (tp & 7) * 2) =
               __float2bfloat16_rn(pv);
         }
         fence_proxy_async_smem();
-        named_bar_sync(1, kEpi);
-        if (t == 0) {
-          mbar_arrive(&pready[slot]);
-          mbar_arrive(&vempty[b]);   // S of this stage has been read
-        }
+        named_bar_sync(2, kGroup);
+        if (tp == 0) mbar_arrive(&pready[ps]);
         if (u > 0 && !take_d(kc - 1)) {
           stop = true;
           break;
@@ -662,145 +813,194 @@ dec_pv_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUten
       }
       if (!stop && n > 0 && !take_d(kc - 1)) stop = true;
       if (stop) break;
-      // ---- write the split: O (thread t = column), the row sums, the reference max
+      // the item's score columns are free for the item three ahead
+      tc_fence_before();
+      named_bar_sync(2, kGroup);
+      if (tp == 0) mbar_arrive(&sfree[sb]);
+
+      // ---- partial result of the split (only if it kept a tile)
+      if (n > 0) {
 #pragma unroll
-      for (int r = 0; r < RB; ++r) {
-        float x = lsum[r];
+        for (int r = 0; r < RB; ++r) {
+          float x = lsum[r];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-        if (lane == 0) lred[warp][r] = x;
-      }
-      named_bar_sync(1, kEpi);
-      const int64_t prow = (int64_t)item * p.rows;
-#pragma unroll
-      for (int r = 0; r < RB; ++r)
-        if (r < R) p.pO[(prow + r) * kTile + t] = O[r];
-      if (t < R) {
-        p.pl[prow + t] = (lred[0][t] + lred[1][t]) + (lred[2][t] + lred[3][t]);
+          for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+          if (lane == 0) lred[wp][r] = x;
+        }
+        named_bar_sync(2, kGroup);
+        const int64_t prow = (int64_t)item * p.rows;
 #pragma unroll
         for (int r = 0; r < RB; ++r)
-          if (r == t) p.pm[prow + t] = mref[r];
+          if (r < R) p.pO[(prow + r) * kTile + tp] = O[r];
+        if (tp < R) {
+          p.pl[prow + tp] = (lred[0][tp] + lred[1][tp]) + (lred[2][tp] + lred[3][tp]);
+#pragma unroll
+          for (int r = 0; r < RB; ++r)
+            if (r == tp) p.pm[prow + tp] = mref[r];
+        }
+        __threadfence();   // the partial is visible before the count below
       }
+      named_bar_sync(2, kGroup);
+      if (tp == 0) {   // the last of the splits of this (sequence, KV head) merges
+        if (n > 0) p.flags[item] = kFlagPart;
+        merge_sh = atom_add_acq_rel(p.done + it.s * p.Hkv + it.kvh, 1) == it.ns - 1;
+      }
+      named_bar_sync(2, kGroup);
+      if (!merge_sh) continue;
+      __threadfence();
+
+      // ---- merge: the splits of this (sequence, KV head) that kept a tile,
+      // in split order: 128 candidates at a time, their list taken in batches
+      // of kE. Thread tp owns column quads g = tp + 128 k (row g / 32,
+      // columns 4 (g % 32) .. +3). Per batch all loads (maxima and sums into
+      // shared memory, the quads' partial outputs into registers) are in
+      // flight together; the running max, the rescale of the accumulators
+      // and the weights are then computed once per row.
+      constexpr int kQ = RB / 4;              // column quads per thread
+      constexpr int kE = 16 / kQ;             // batch: partial results whose loads overlap
+      float4 acc[kQ];
+#pragma unroll
+      for (int k = 0; k < kQ; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (tp < RB) {
+        msh[tp] = -INFINITY;
+        lsh[tp] = 0.f;
+      }
+      for (int b0 = 0; b0 < it.ns; b0 += kGroup) {
+        const int qq = b0 + tp;
+        const int64_t x = first + (int64_t)qq * p.Hkv;
+        const bool has = qq < it.ns && (__ldcg(p.flags + x) & kFlagPart);
+        const unsigned bal = __ballot_sync(0xffffffffu, has);
+        if (lane == 0) wcnt[wp] = __popc(bal);
+        named_bar_sync(2, kGroup);
+        int off = 0;
+        for (int w = 0; w < wp; ++w) off += wcnt[w];
+        const int cnt = (wcnt[0] + wcnt[1]) + (wcnt[2] + wcnt[3]);
+        if (has) clist[off + __popc(bal & ((1u << lane) - 1u))] = (int)(x - first);
+        named_bar_sync(2, kGroup);
+        for (int e0 = 0; e0 < cnt; e0 += kE) {
+          const int E = min(kE, cnt - e0);
+          // the batch's maxima, sums and partial outputs, all loads in flight
+          for (int y = tp; y < E * R; y += kGroup) {
+            const int e = y / R, r = y - e * R;
+            const int64_t prow = (first + clist[e0 + e]) * p.rows;
+            pmsh[e][r] = __ldcg(p.pm + prow + r);
+            plsh[e][r] = __ldcg(p.pl + prow + r);
+          }
+          float4 v[kE][kQ];
+#pragma unroll
+          for (int e = 0; e < kE; ++e) {
+            const int64_t prow = (first + clist[e0 + (e < E ? e : 0)]) * p.rows;
+#pragma unroll
+            for (int k = 0; k < kQ; ++k) {
+              const int g = tp + kGroup * k, r = g >> 5;
+              v[e][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (e < E && r < R)
+                v[e][k] = __ldcg(reinterpret_cast<const float4 *>(p.pO + (prow + r) * kTile) + (g & 31));
+            }
+          }
+          named_bar_sync(2, kGroup);
+          if (tp < R) {   // running max, rescale, sum and weights of row tp
+            const float mo = msh[tp];
+            float mn = mo;
+            for (int e = 0; e < E; ++e) mn = fmaxf(mn, pmsh[e][tp]);
+            const float sc = mo == -INFINITY ? 0.f : ex2_approx(mo - mn);
+            float l = lsh[tp] * sc;
+            for (int e = 0; e < E; ++e) {
+              const float w = pmsh[e][tp] == -INFINITY ? 0.f : ex2_approx(pmsh[e][tp] - mn);
+              wsh[e][tp] = w;
+              l = fmaf(plsh[e][tp], w, l);
+            }
+            msh[tp] = mn;
+            lsh[tp] = l;
+            scsh[tp] = sc;
+          }
+          named_bar_sync(2, kGroup);
+#pragma unroll
+          for (int k = 0; k < kQ; ++k) {
+            const int g = tp + kGroup * k, r = g >> 5;
+            if (r < R) {
+              const float sc = scsh[r];
+              float4 a = make_float4(acc[k].x * sc, acc[k].y * sc, acc[k].z * sc, acc[k].w * sc);
+#pragma unroll
+              for (int e = 0; e < kE; ++e) {
+                const float w = e < E ? wsh[e][r] : 0.f;
+                a.x = fmaf(v[e][k].x, w, a.x);
+                a.y = fmaf(v[e][k].y, w, a.y);
+                a.z = fmaf(v[e][k].z, w, a.z);
+                a.w = fmaf(v[e][k].w, w, a.w);
+              }
+              acc[k] = a;
+            }
+          }
+          named_bar_sync(2, kGroup);   // the staged batch is rewritten next
+        }
+      }
+      __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+      const int total_q = p.cu_q[p.n_seqs];
+#pragma unroll
+      for (int k = 0; k < kQ; ++k) {
+        const int g = tp + kGroup * k, r = g >> 5;
+        if (r < R) {
+          const int h = it.kvh * p.group + r / it.Lq, qi = r % it.Lq;
+          const float l = lsh[r], inv = l > 0.f ? 1.f / l : 0.f;
+          uint2 o;
+          o.x = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
+          o.y = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
+          *reinterpret_cast<uint2 *>(out + ((size_t)(it.aq + qi) * p.Hq + h) * kTile + 4 * (g & 31)) = o;
+        }
+      }
+      if (p.lse && tp < R) {
+        const int h = it.kvh * p.group + tp / it.Lq, qi = tp % it.Lq;
+        p.lse[(size_t)h * total_q + it.aq + qi] = (msh[tp] + log2f(lsh[tp])) * kLn2;
+      }
+      named_bar_sync(2, kGroup);   // msh / lsh are reset by the next merge
     }
     if (stop) abort_sh = 1;
+    if (abort_sh && tp == 0) atomicExch(const_cast<int32_t *>(gabort), 1);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (abort_sh && t == 0) atomicOr(&p.ws->status, kStatusTimeout);
-  if (warp == 5) tmem_dealloc(tmem, 2 * N < 32 ? 32 : 2 * N);
-}
-
-// ============================================================ 3: merge
-
-// One CTA per (sequence, query slot, query head); thread t = column t%128 of
-// the splits q with q%4 == t/128, the four groups added at the end.
-__global__ void __launch_bounds__(4 * kTile) dec_combine_kernel(const __grid_constant__ DecParams p) {
-  __shared__ float red[4 * kTile / 32];
-  __shared__ float part[3][kTile], lpart[4];
-  grid_dep_wait();
-  if (p.dw->total_items == 0) return;
-  const int per_seq = p.max_q * p.Hq;
-  const int s = blockIdx.x / per_seq, rem = blockIdx.x - s * per_seq;
-  const int qi = rem / p.Hq, h = rem - qi * p.Hq;
-  const int aq = p.cu_q[s], Lq = p.cu_q[s + 1] - aq;
-  if (qi >= Lq) return;
-  const int t = threadIdx.x, c = t & (kTile - 1), grp = t >> 7, lane = t & 31, warp = t >> 5;
-  const int Lk = p.cu_k[s + 1] - p.cu_k[s];
-  const int nk = (Lk + kTile - 1) / kTile, ns = (nk + p.split - 1) / p.split;
-  const int kvh = h / p.group, r = (h - kvh * p.group) * Lq + qi;
-  const int64_t it0 = (int64_t)p.item_off[s] + kvh;   // split q is item it0 + q * Hkv
-  const int64_t H = p.Hkv;
-  float m = -INFINITY;
-  for (int q = t; q < ns; q += 4 * kTile) m = fmaxf(m, p.pm[(it0 + q * H) * p.rows + r]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0) red[warp] = m;
-  __syncthreads();
-  m = red[0];
-#pragma unroll
-  for (int w = 1; w < 4 * kTile / 32; ++w) m = fmaxf(m, red[w]);
-  float acc = 0.f, l = 0.f;
-#pragma unroll 4
-  for (int q = grp; q < ns; q += 4) {
-    const int64_t ii = it0 + q * H;
-    const float mi = p.pm[ii * p.rows + r];
-    if (mi == -INFINITY) continue;   // no kept tile of this split for the row
-    const float w = ex2_approx(mi - m);
-    l = fmaf(p.pl[ii * p.rows + r], w, l);
-    acc = fmaf(p.pO[(ii * p.rows + r) * kTile + c], w, acc);
-  }
-  if (grp > 0) part[grp - 1][c] = acc;
-  if (c == 0) lpart[grp] = l;
-  __syncthreads();
-  if (grp == 0) {
-    acc += (part[0][c] + part[1][c]) + part[2][c];
-    l = (lpart[0] + lpart[1]) + (lpart[2] + lpart[3]);
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
-    out[((size_t)(aq + qi) * p.Hq + h) * kTile + c] = __float2bfloat16_rn(acc * inv);
-    if (p.lse && t == 0) p.lse[(size_t)h * p.cu_q[p.n_seqs] + aq + qi] = (m + log2f(l)) * kLn2;
-  }
+  if (warp == 10) tmem_dealloc(tmem, 512);
 }
 
 // ============================================================ launchers
 
-namespace {
-// K / V ring, then the query rows (scores) or P (P V), fp32, 4..32 rows
-size_t dec_smem_bytes(int rows) {
-  return (size_t)kStages * kTileBytes + 1024 + (size_t)((rows + 3) & ~3) * kTile * 4;
+cudaError_t launch_decode(const DecParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                          int sm_count, cudaStream_t stream) {
+  const int grid = (int)(p.max_items < sm_count ? p.max_items : sm_count);
+  cudaError_t e = launch_dependent(dec_prologue_kernel, 1, 1024, 0, stream, p);
+  if (e != cudaSuccess) return e;
+  if (p.rows <= 4)
+    return launch_dependent(dec_kernel<4>, grid, kDecThreadsAll, DecCfg<4>::kSmem, stream, p, tk, tv);
+  if (p.rows <= 8)
+    return launch_dependent(dec_kernel<8>, grid, kDecThreadsAll, DecCfg<8>::kSmem, stream, p, tk, tv);
+  if (p.rows <= 16)
+    return launch_dependent(dec_kernel<16>, grid, kDecThreadsAll, DecCfg<16>::kSmem, stream, p, tk, tv);
+  return launch_dependent(dec_kernel<32>, grid, kDecThreadsAll, DecCfg<32>::kSmem, stream, p, tk, tv);
 }
-// V ring with the staged scores, then two P buffers (N = RB rounded up to 16)
-size_t pv_smem_bytes(int RB) {
-  const int N = RB < 16 ? 16 : RB;
-  return (size_t)kStages * (kTileBytes + RB * kTile * 4) + 1024 + 2 * (size_t)N * 256;
+
+int decode_split(int rows) { return rows <= 16 ? DecCfg<16>::kSplit : DecCfg<32>::kSplit; }
+
+namespace {
+// The register split adds up only if every thread starts with kRegsLaunch.
+template <int RB>
+cudaError_t prepare_one() {
+  cudaError_t e = cudaFuncSetAttribute(dec_kernel<RB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)DecCfg<RB>::kSmem);
+  cudaFuncAttributes fa{};
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, dec_kernel<RB>);
+  if (e == cudaSuccess && fa.numRegs != (int)kRegsLaunch) e = cudaErrorInvalidKernelImage;
+  return e;
 }
 }  // namespace
 
-cudaError_t launch_decode(const DecParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                          int sm_count, cudaStream_t stream) {
-  const int64_t max_tiles = p.total_k / kTile + p.n_seqs;
-  const int64_t max_items = (int64_t)p.Hkv * (max_tiles / p.split + p.n_seqs);
-  const int grid = (int)(max_items < 4LL * sm_count ? max_items : 4LL * sm_count);
-  const int block = kDecScoreThreads + 64;
-  dec_prologue_kernel<<<1, 1024, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (p.rows <= 16)
-    e = launch_dependent(dec_scores_kernel<16>, grid, block, dec_smem_bytes(16), stream, p, tk);
-  else
-    e = launch_dependent(dec_scores_kernel<32>, grid, block, dec_smem_bytes(32), stream, p, tk);
-  if (e != cudaSuccess) return e;
-  if (p.rows <= 4)
-    e = launch_dependent(dec_pv_kernel<4>, grid, block, pv_smem_bytes(4), stream, p, tv);
-  else if (p.rows <= 8)
-    e = launch_dependent(dec_pv_kernel<8>, grid, block, pv_smem_bytes(8), stream, p, tv);
-  else if (p.rows <= 16)
-    e = launch_dependent(dec_pv_kernel<16>, grid, block, pv_smem_bytes(16), stream, p, tv);
-  else
-    e = launch_dependent(dec_pv_kernel<32>, grid, block, pv_smem_bytes(32), stream, p, tv);
-  if (e != cudaSuccess) return e;
-  return launch_dependent(dec_combine_kernel, p.n_seqs * p.max_q * p.Hq, 4 * kTile, 0, stream, p);
-}
-
 cudaError_t prepare_decode() {
-  const int smem = (int)dec_smem_bytes(kDecMaxRows);
-  cudaError_t e =
-      cudaFuncSetAttribute(dec_scores_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(dec_scores_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(dec_pv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)pv_smem_bytes(4));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(dec_pv_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)pv_smem_bytes(8));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(dec_pv_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)pv_smem_bytes(16));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(dec_pv_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)pv_smem_bytes(32));
+  cudaError_t e = prepare_one<4>();
+  if (e == cudaSuccess) e = prepare_one<8>();
+  if (e == cudaSuccess) e = prepare_one<16>();
+  if (e == cudaSuccess) e = prepare_one<32>();
   return e;
 }
 

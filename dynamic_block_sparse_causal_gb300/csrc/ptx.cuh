@@ -101,6 +101,13 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *map, uint64_t
       : "memory");
 }
 
+// Prefetch one tile of a tensor into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_3d(const void *map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

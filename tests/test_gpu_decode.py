@@ -101,9 +101,9 @@ def test_decode_batch_of_four_32k():
     _gpu.compare(p, g)
 
 
-def test_decode_sixteen_tile_splits():
-    """Enough keys that the library splits them 16 tiles at a time (smaller
-    batches get 8-tile splits): 16 KV heads x 80K keys."""
+def test_decode_many_work_items():
+    """Several work items per SM: 16 KV heads x 80K keys in two sequences,
+    so the CTAs claim items from both sequences in turn."""
     base = gi.packed("dec16", [40000, 40064], Hq=32, Hkv=16, seed=4, window=2.0,
                      window_period=4096, window_len=512)
     p = gi.chunk(base, [1, 2])
@@ -111,6 +111,21 @@ def test_decode_sixteen_tile_splits():
         g, st = run_decode(p, lam)
         assert st == 0
         print(lam, _gpu.compare(p, g))
+
+
+@pytest.mark.parametrize("Hq,L,lq", [(4, 170000, 1), (8, 70000, 4)])
+def test_decode_lookback_over_many_splits(Hq, L, lq):
+    """One long sequence on one KV head: the last work items have more than
+    128 earlier splits (8-tile splits at 4 query rows, 4-tile splits at 32),
+    so the look-back for the running max spans several windows of earlier
+    splits and stops at published inclusive prefixes."""
+    base = gi.packed("declong", [L], Hq=Hq, Hkv=1, seed=9, window=2.0, window_period=4096,
+                     window_len=512)
+    p = gi.chunk(base, [lq])
+    for lam in (0.005, 0.0):
+        g, st = run_decode(p, lam)
+        assert st == 0
+        print(Hq, L, lq, lam, _gpu.compare(p, g))
 
 
 def test_decode_batch_with_query_free_sequences():
