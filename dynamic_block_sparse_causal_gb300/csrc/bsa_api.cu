@@ -42,6 +42,7 @@ struct Buffer {
 struct StreamState {
   std::mutex mu;
   Buffer ws, imp, dec;
+  uint32_t dec_epoch = 0;   // decode calls on this stream (tags their per-call state)
 };
 
 std::mutex g_mu;   // guards g_streams, g_devices and g_encode
@@ -123,13 +124,16 @@ bsa_status_t scratch_for(StreamState *ss, cudaStream_t stream, size_t bytes, Wor
 }
 
 // Block-importance or decode tables of a stream, grown stream-ordered. Under ss->mu.
-bsa_status_t table_for(Buffer &s, cudaStream_t stream, size_t bytes, void **out) {
+bsa_status_t table_for(Buffer &s, cudaStream_t stream, size_t bytes, void **out,
+                       bool *grown = nullptr) {
+  if (grown) *grown = false;
   if (s.bytes < bytes) {
     void *p = nullptr;
     if (cudaMallocAsync(&p, bytes, stream) != cudaSuccess) return BSA_ERR_NO_MEMORY;
     if (s.ptr && cudaFreeAsync(s.ptr, stream) != cudaSuccess) return BSA_ERR_CUDA;
     s.ptr = p;
     s.bytes = bytes;
+    if (grown) *grown = true;
   }
   *out = s.ptr;
   return BSA_OK;
@@ -325,10 +329,19 @@ bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
   const int split = bsa::decode_split(rows);
   const bsa::DecLayout layout = bsa::DecLayout::make(n_seqs, Hkv, rows, total_k, split);
   void *buf = nullptr;
-  if ((st = table_for(ss->dec, stream, layout.bytes, &buf)) != BSA_OK) return st;
+  bool grown = false;
+  if ((st = table_for(ss->dec, stream, layout.bytes, &buf, &grown)) != BSA_OK) return st;
+  // epoch-tagged state: a new buffer starts at zero (no epoch), and so does
+  // the buffer once the count of calls wraps
+  if (++ss->dec_epoch == 0) {
+    ss->dec_epoch = 1;
+    grown = true;
+  }
+  if (grown && cudaMemsetAsync(buf, 0, ss->dec.bytes, stream) != cudaSuccess) return BSA_ERR_CUDA;
   char *base = static_cast<char *>(buf);
   bsa::DecParams p{};
   p.dw = static_cast<bsa::DecWorkspace *>(buf);
+  p.epoch = ss->dec_epoch;
   p.ws = ws;
   p.q = q;
   p.cu_q = cu_seqlens_q;
@@ -337,8 +350,8 @@ bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
   p.bm_off = reinterpret_cast<const int64_t *>(base + layout.bm_off);
   p.flags = reinterpret_cast<uint32_t *>(base + layout.flags);
   p.done = reinterpret_cast<int32_t *>(base + layout.done);
-  p.agg = reinterpret_cast<float *>(base + layout.agg);
-  p.incl = reinterpret_cast<float *>(base + layout.incl);
+  p.agg = reinterpret_cast<uint64_t *>(base + layout.agg);
+  p.incl = reinterpret_cast<uint64_t *>(base + layout.incl);
   p.pO = reinterpret_cast<float *>(base + layout.pO);
   p.pm = reinterpret_cast<float *>(base + layout.pm);
   p.pl = reinterpret_cast<float *>(base + layout.pl);

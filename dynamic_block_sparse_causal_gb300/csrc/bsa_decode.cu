@@ -31,10 +31,12 @@
 //   merge    the item of a (sequence, KV head) that finishes last (a counter)
 //            merges the partial results of the splits that kept a tile; no
 //            item waits for that.
-// Published maxima need no fences: the prologue fills them with NaN, a
-// writer stores the value (never NaN) with one relaxed 32-bit store, and a
-// reader polls until it reads a number. An item waits only for items of lower
-// index; those were claimed earlier by CTAs that are running and publish
+// Published maxima need no fences: each is one relaxed 64-bit store of the
+// value and the call's epoch (a per-stream count of calls), and a reader polls
+// until it reads its own call's epoch. The first CTA to arrive writes the
+// call's tables (a block-wide scan over the sequences) while the others wait
+// for it; nothing else needs clearing between calls. An item waits only for
+// items of lower index; those were claimed earlier by CTAs that are running and publish
 // their maxima before they wait for anything outside their CTA, so the waits
 // end; each is bounded by the wait limit all the same. Decisions equal the sequential walk's; outputs equal
 // the online softmax over the kept tiles up to rounding order. The work is
@@ -55,7 +57,6 @@ constexpr uint32_t kTileBytes = 32768;   // 128 keys x 128 bf16
 constexpr uint32_t kBoxBytes = 16384;    // one 128-row x 128-byte TMA box
 constexpr float kLn2 = 0.6931471805599453f;
 
-constexpr uint32_t kFlagPart = 1;   // a work item's partial output is written (it kept a tile)
 
 struct DecItem {
   int s, kvh, q, j0, j1, aq, Lq, ak, Lk, ns;
@@ -83,23 +84,32 @@ __device__ __forceinline__ void decode_item(const DecParams &p, int item, DecIte
   it.j1 = min(nk, it.j0 + p.split);
 }
 
+// One 128-key tile of K or V (both 64-column boxes); K and V are read once,
+// so their lines leave L2 first and the per-item tables stay.
 __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, uint64_t *bar,
-                                          int head, int row) {
+                                          int head, int row, uint64_t policy) {
   mbar_expect_tx(bar, kTileBytes);
-  tma_load_3d(dst, map, bar, 0, head, row);
-  tma_load_3d(dst + kBoxBytes, map, bar, 64, head, row);
+  tma_load_3d_hint(dst, map, bar, 0, head, row, policy);
+  tma_load_3d_hint(dst + kBoxBytes, map, bar, 64, head, row, policy);
 }
 
-// Four published maxima at once (16-byte aligned); several can be in flight.
-__device__ __forceinline__ float4 ld_volatile4(const float *a) {
-  float4 v;
-  asm volatile("ld.volatile.global.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "l"(a));
+// Two published (epoch, value) words at once (16-byte aligned); several can
+// be in flight.
+__device__ __forceinline__ void ld_volatile_pair(const uint64_t *a, uint64_t &x, uint64_t &y) {
+  asm volatile("ld.volatile.global.v2.u64 {%0,%1}, [%2];" : "=l"(x), "=l"(y) : "l"(a));
+}
+// Publish a maximum: one relaxed 64-bit store of (epoch, f32 bits).
+__device__ __forceinline__ void publish(uint64_t *a, uint32_t epoch, float v) {
+  const uint64_t w = ((uint64_t)epoch << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(w) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *a) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
   return v;
 }
-__device__ __forceinline__ void st_relaxed(float *a, float v) {
-  asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(a), "f"(v) : "memory");
+__device__ __forceinline__ void st_release_u32(uint32_t *a, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
 }
 __device__ __forceinline__ int atom_add_acq_rel(int32_t *a, int v) {
   int old;
@@ -126,41 +136,39 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, uint64_
   }
 }
 
-// The first R of RB published maxima at a (16-byte aligned, RB a multiple
-// of 4) into v, loads in flight together.
+// The first R of RB published (epoch, value) words at a (16-byte aligned, RB
+// even) into w, loads in flight together.
 template <int RB>
-__device__ __forceinline__ void load_maxima(const float *a, int R, float (&v)[RB]) {
+__device__ __forceinline__ void load_maxima(const uint64_t *a, int R, uint64_t (&w)[RB]) {
 #pragma unroll
-  for (int r = 0; r < RB; r += 4) {
-    float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    if (r < R) x = ld_volatile4(a + r);
-    v[r] = x.x;
-    v[r + 1] = x.y;
-    v[r + 2] = x.z;
-    v[r + 3] = x.w;
+  for (int r = 0; r < RB; r += 2) {
+    w[r] = w[r + 1] = 0;
+    if (r < R) ld_volatile_pair(a + r, w[r], w[r + 1]);
   }
 }
 template <int RB>
-__device__ __forceinline__ bool all_published(const float (&v)[RB], int R) {
+__device__ __forceinline__ bool all_published(const uint64_t (&w)[RB], int R, uint32_t epoch) {
   bool ok = true;
 #pragma unroll
-  for (int r = 0; r < RB; ++r) ok = ok && (r >= R || !isnan(v[r]));
+  for (int r = 0; r < RB; ++r) ok = ok && (r >= R || (uint32_t)(w[r] >> 32) == epoch);
   return ok;
 }
+__device__ __forceinline__ float value_of(uint64_t w) { return __uint_as_float((uint32_t)w); }
 
-// Wait until another CTA has published the first R maxima at a (slots hold
-// NaN until then); false on a CTA or grid abort, or past the limit.
+// Wait until the first R maxima at a carry this call's epoch; false on a CTA
+// or grid abort, or past the limit.
 template <int RB>
-__device__ __forceinline__ bool wait_maxima(const float *a, int R, float (&v)[RB], uint64_t limit,
-                                            volatile int *abort, const volatile int32_t *gabort) {
-  load_maxima<RB>(a, R, v);
-  if (all_published<RB>(v, R)) return true;
+__device__ __forceinline__ bool wait_maxima(const uint64_t *a, int R, uint64_t (&w)[RB], uint32_t epoch,
+                                            uint64_t limit, volatile int *abort,
+                                            const volatile uint32_t *gabort) {
+  load_maxima<RB>(a, R, w);
+  if (all_published<RB>(w, R, epoch)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     __nanosleep(64);
-    load_maxima<RB>(a, R, v);
-    if (all_published<RB>(v, R)) return true;
-    if (*abort || *gabort) return false;
+    load_maxima<RB>(a, R, w);
+    if (all_published<RB>(w, R, epoch)) return true;
+    if (*abort || *gabort == epoch) return false;
     if (globaltimer_ns() - t0 > limit) return false;
   }
 }
@@ -173,63 +181,9 @@ __device__ __forceinline__ float warp_max(float x) {
   return __int_as_float(k >= 0 ? k : k ^ 0x7FFFFFFF);
 }
 
-// A published maximum is never NaN (NaN marks "not yet published").
-__device__ __forceinline__ float publishable(float m) { return isnan(m) ? -INFINITY : m; }
+
 
 }  // namespace
-
-// ============================================================ prologue
-
-__global__ void __launch_bounds__(1024) dec_prologue_kernel(const __grid_constant__ DecParams p) {
-  __shared__ int s_bad;
-  const int tid = threadIdx.x;
-  grid_dep_launch();   // the decode kernel may set up meanwhile; it waits for this grid
-  grid_dep_wait();     // the previous kernel on the stream (possibly a decode) is done
-  if (tid == 0)
-    s_bad = p.cu_q[0] != 0 || p.cu_k[0] != 0 || (int64_t)p.cu_k[p.n_seqs] != p.total_k;
-  __syncthreads();
-  for (int s = tid; s < p.n_seqs; s += blockDim.x) {
-    const int Lq = p.cu_q[s + 1] - p.cu_q[s], Lk = p.cu_k[s + 1] - p.cu_k[s];
-    if (Lq < 0 || Lk < 0 || Lq > p.max_q || (p.causal && Lk < Lq) || (Lq > 0 && Lk == 0))
-      atomicOr(&s_bad, 1);
-  }
-  __syncthreads();
-  if (tid == 0) {
-    bool bad = s_bad != 0;
-    long long items = 0, words = 0;
-    int64_t *bm_off = const_cast<int64_t *>(p.bm_off);
-    int32_t *item_off = const_cast<int32_t *>(p.item_off);
-    for (int s = 0; s < p.n_seqs && !bad; ++s) {
-      const int Lq = p.cu_q[s + 1] - p.cu_q[s], Lk = p.cu_k[s + 1] - p.cu_k[s];
-      const long long nk = (Lk + kTile - 1) / kTile, nq = (Lq + kTile - 1) / kTile;
-      item_off[s] = (int32_t)min(items, (long long)INT_MAX);
-      bm_off[s] = words;
-      if (Lq > 0) items += (long long)p.Hkv * ((nk + p.split - 1) / p.split);
-      words += (long long)p.Hq * nq * ((nk + 31) / 32);
-    }
-    item_off[p.n_seqs] = (int32_t)min(items, (long long)INT_MAX);
-    bm_off[p.n_seqs] = words;
-    if (items > p.max_items) bad = true;
-    p.dw->total_items = bad ? 0 : (int32_t)items;
-    p.dw->next_item = 0;
-    p.dw->abort = 0;
-    if (bad) atomicOr(&p.ws->status, kStatusBadSeqlens);
-    s_bad = bad;
-  }
-  __syncthreads();
-  if (s_bad) return;
-  // the decode kernel ORs skip bits into the bitmap, counts finished items and
-  // publishes maxima into slots that hold NaN until then
-  if (p.bitmap)
-    for (int64_t w = tid; w < p.bm_off[p.n_seqs]; w += blockDim.x) p.bitmap[w] = 0u;
-  const int items = p.dw->total_items;
-  for (int x = tid; x < items; x += blockDim.x) p.flags[x] = 0u;
-  for (int x = tid; x < p.n_seqs * p.Hkv; x += blockDim.x) p.done[x] = 0;
-  for (int64_t x = tid; x < (int64_t)items * p.mpitch; x += blockDim.x) {
-    p.agg[x] = __int_as_float(0x7fc00000);
-    p.incl[x] = __int_as_float(0x7fc00000);
-  }
-}
 
 // ============================================================ decode
 
@@ -285,20 +239,93 @@ struct DecCfg {
 constexpr int kGroup = 128;          // threads of the score group and of the P V group
 constexpr int kDecThreadsAll = 384;  // two groups + K producer, V producer, two MMA warps
 // Registers per thread: the launch gives every thread kRegsLaunch; the
-// producer / MMA warpgroup gives most of its share to the P V group.
-constexpr uint32_t kRegsLaunch = 168, kRegsIssue = 64, kRegsPV = 256;
-static_assert(kGroup * (kRegsLaunch + kRegsPV + kRegsIssue) <= kDecThreadsAll * kRegsLaunch,
+// producer / MMA warpgroup gives most of its share to the two groups.
+constexpr uint32_t kRegsLaunch = 168, kRegsIssue = 64, kRegsScore = 184, kRegsPV = 256;
+static_assert(kGroup * (kRegsScore + kRegsPV + kRegsIssue) <= kDecThreadsAll * kRegsLaunch,
               "register split above the launch allocation");
 constexpr int kMaxSplitRB = 128;     // kSplit x RB: tile-max entries of one item
 
 }  // namespace
 
+// The call's tables, written by all threads of the first CTA to arrive: per
+// sequence its first work item and first skip-bitmap word (a block-wide scan
+// over the sequences, NT at a time), the checks of the lengths on the
+// device, the item count, and the zeroed counters.
+template <int NT>
+__device__ void dec_setup(const DecParams &p, long long (&wsum)[NT / 32][2], long long (&carry)[2],
+                          int &bad_sh) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  if (t == 0) {
+    bad_sh = p.cu_q[0] != 0 || p.cu_k[0] != 0 || (int64_t)p.cu_k[p.n_seqs] != p.total_k;
+    carry[0] = carry[1] = 0;
+  }
+  __syncthreads();
+  int32_t *item_off = const_cast<int32_t *>(p.item_off);
+  int64_t *bm_off = const_cast<int64_t *>(p.bm_off);
+  for (int b0 = 0; b0 < p.n_seqs; b0 += NT) {
+    const int s = b0 + t;
+    long long ni = 0, nw = 0;   // this sequence's work items and bitmap words
+    if (s < p.n_seqs) {
+      const int Lq = p.cu_q[s + 1] - p.cu_q[s], Lk = p.cu_k[s + 1] - p.cu_k[s];
+      if (Lq < 0 || Lk < 0 || Lq > p.max_q || (p.causal && Lk < Lq) || (Lq > 0 && Lk == 0)) {
+        atomicOr(&bad_sh, 1);
+      } else {
+        const long long nk = (Lk + kTile - 1) / kTile, nq = (Lq + kTile - 1) / kTile;
+        if (Lq > 0) ni = (long long)p.Hkv * ((nk + p.split - 1) / p.split);
+        nw = (long long)p.Hq * nq * ((nk + 31) / 32);
+      }
+    }
+    long long si = ni, sw = nw;   // inclusive scans within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long xi = __shfl_up_sync(0xffffffffu, si, o);
+      const long long xw = __shfl_up_sync(0xffffffffu, sw, o);
+      if (lane >= o) {
+        si += xi;
+        sw += xw;
+      }
+    }
+    if (lane == 31) {
+      wsum[warp][0] = si;
+      wsum[warp][1] = sw;
+    }
+    __syncthreads();
+    long long oi = carry[0], ow = carry[1];
+    for (int w = 0; w < warp; ++w) {
+      oi += wsum[w][0];
+      ow += wsum[w][1];
+    }
+    if (s < p.n_seqs) {
+      item_off[s] = (int32_t)min(oi + si - ni, (long long)INT_MAX);
+      bm_off[s] = ow + sw - nw;
+    }
+    __syncthreads();
+    if (t == 0)
+      for (int w = 0; w < NT / 32; ++w) {
+        carry[0] += wsum[w][0];
+        carry[1] += wsum[w][1];
+      }
+    __syncthreads();
+  }
+  if (t == 0) {
+    const long long items = carry[0];
+    item_off[p.n_seqs] = (int32_t)min(items, (long long)INT_MAX);
+    bm_off[p.n_seqs] = carry[1];
+    const bool bad = bad_sh != 0 || items > p.max_items;
+    p.dw->total_items = bad ? 0 : (int32_t)items;
+    p.dw->next_item = 0;
+    if (bad) atomicOr(&p.ws->status, kStatusBadSeqlens);
+  }
+  for (int x = t; x < p.n_seqs * p.Hkv; x += NT) p.done[x] = 0;
+  __syncthreads();
+}
+
 // Roles:
 //   warps 0-3   score group: the scores of the split from TMEM (thread =
-//               key), per-tile row maxima, the split maxima published
-//   warps 4-7   P V group: look-back, decisions, skip bits, P of the kept
-//               tiles (thread = key), O (thread = head-dim column), partial
-//               results, the merge
+//               key), per-tile row maxima, the split maxima published; the
+//               look-back, the decisions, the kept list and the skip bits
+//   warps 4-7   P V group: P of the kept tiles (thread = key), O (thread =
+//               head-dim column), partial results, the merge
 //   warp 8      claims items, stages their query rows (the score MMA's B
 //               operand); lane 0: TMA producer of the K ring
 //   warp 9      lane 0: TMA producer of the V ring (kept tiles only)
@@ -328,8 +355,10 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
   __shared__ float pmsh[16][RB], plsh[16][RB], wsh[16][RB];
   __shared__ float msh[RB], lsh[RB], scsh[RB];
   __shared__ uint64_t itfull[4], itempty[4], kfull[KST], kempty[KST], vfull[VST], vempty[VST],
-      qready[2], qfree[2], sfull[3], sfree[3], mready[3], lready[2], lfree[2], pready[2], pfree[2],
+      qready[2], qfree[2], sfull[3], sfree[3], lready[2], lfree[2], pready[2], pfree[2],
       dfull[2], dempty[2], drain[2];
+  __shared__ long long wsum[kDecThreadsAll / 32][2], carry[2];
+  __shared__ int bad_sh, owner_sh;
   __shared__ uint32_t tmem_sh;
   __shared__ volatile int abort_sh;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -352,13 +381,12 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
     for (int b = 0; b < 3; ++b) {
       mbar_init(&sfull[b], 1);
       mbar_init(&sfree[b], 1);
-      mbar_init(&mready[b], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&qready[b], 1);
       mbar_init(&qfree[b], 1);
       mbar_init(&lready[b], 1);
-      mbar_init(&lfree[b], 2);   // V producer, P V MMA
+      mbar_init(&lfree[b], 3);   // V producer, P V MMA, P V group
       mbar_init(&pready[b], 1);
       mbar_init(&pfree[b], 1);
       mbar_init(&dfull[b], 1);
@@ -380,14 +408,34 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_sh;
-  grid_dep_wait();     // tables of the prologue
+  grid_dep_wait();     // the previous kernel on the stream is done
   grid_dep_launch();
-  const int total = p.dw->total_items;
   const uint64_t limit = p.wait_limit_ns;
-  const volatile int32_t *gabort = &p.dw->abort;
+  const volatile uint32_t *gabort = &p.dw->abort;   // == epoch: a CTA gave up
+  // the call's tables: the first CTA to arrive writes them, the others wait
+  if (t == 0) owner_sh = atomicExch(&p.dw->setup_owner, p.epoch) != p.epoch;
+  __syncthreads();
+  if (owner_sh) {
+    dec_setup<kDecThreadsAll>(p, wsum, carry, bad_sh);
+    if (t == 0) {
+      __threadfence();
+      st_release_u32(&p.dw->setup_done, p.epoch);
+    }
+  } else if (t == 0) {
+    bool ok = ld_acquire_u32(&p.dw->setup_done) == p.epoch;
+    const uint64_t t0 = globaltimer_ns();
+    while (!ok && globaltimer_ns() - t0 <= limit) {
+      __nanosleep(100);
+      ok = ld_acquire_u32(&p.dw->setup_done) == p.epoch;
+    }
+    if (!ok) abort_sh = 1;
+  }
+  __syncthreads();
+  const int total = abort_sh ? 0 : __ldcg(&p.dw->total_items);
 
   if (warp >= 8) {
     reg_dealloc<kRegsIssue>();
+    const uint64_t pol = policy_evict_first();
     if (warp == 8) {
       // ---------------------------------------------------- claims, Q rows, K producer
       const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
@@ -401,7 +449,9 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
         bool ok = true;
         if (lane == 0) {
           ok = wait_bar(&itempty[slot], ((i >> 2) & 1) ^ 1, limit, &abort_sh);
-          if (ok && !abort_sh && !*gabort) {
+          // claims only (never a fixed item per CTA): every claimed item then
+          // belongs to a CTA that is running, even when other grids hold SMs
+          if (ok && !abort_sh && *gabort != p.epoch) {
             item = atomicAdd(&p.dw->next_item, 1);
             if (item >= total) item = -1;
           }
@@ -417,6 +467,19 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
         if (!ok || item < 0) break;
         DecItem it;
         decode_item(p, item, it);
+        // K loads into ring stages that are free right now go first (at the
+        // start, the whole ring), the rest after the query rows are staged
+        int jn = it.j0;
+        if (lane == 0) {
+          for (; jn < it.j1; ++jn, ++kc) {
+            const uint32_t b = kc % KST;
+            if (!mbar_test_wait(smem_u32(&kempty[b]), ((kc / KST) & 1) ^ 1)) break;
+            if ((int)kc != p.debug_drop_k_load) {
+              load_tile(base + b * kTileBytes, &tk, &kfull[b], it.kvh, it.ak + jn * kTile, pol);
+              last_issue[b] = (int)kc;
+            }
+          }
+        }
         // B operand: query row r at its 128-byte-swizzled K-major position
         const int R = p.group * it.Lq;
         uint8_t *qb = base + C::kQOff + par * C::kQBytes;
@@ -434,11 +497,11 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
         bool okk = true;
         if (lane == 0) {
           mbar_arrive(&qready[par]);
-          for (int j = it.j0; j < it.j1; ++j, ++kc) {
+          for (int j = jn; j < it.j1; ++j, ++kc) {
             const uint32_t b = kc % KST;
             if (!(okk = wait_bar(&kempty[b], ((kc / KST) & 1) ^ 1, limit, &abort_sh))) break;
             if ((int)kc != p.debug_drop_k_load) {
-              load_tile(base + b * kTileBytes, &tk, &kfull[b], it.kvh, it.ak + j * kTile);
+              load_tile(base + b * kTileBytes, &tk, &kfull[b], it.kvh, it.ak + j * kTile, pol);
               last_issue[b] = (int)kc;
             }
           }
@@ -476,7 +539,7 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
             const uint32_t b = vc % VST;
             if (!(ok = wait_bar(&vempty[b], ((vc / VST) & 1) ^ 1, limit, &abort_sh))) break;
             load_tile(base + C::kVOff + b * kTileBytes, &tv, &vfull[b], it.kvh,
-                      it.ak + klist[par][u] * kTile);
+                      it.ak + klist[par][u] * kTile, pol);
             last_issue[b] = (int)vc;
           }
           if (!ok) break;
@@ -573,10 +636,11 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
       }
     }
   } else if (warp < 4) {
+    reg_alloc<kRegsScore>();
     // ---------------------------------------------------- score group
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     for (uint32_t i = 0;; ++i) {
-      const uint32_t slot = i & 3, sb = i % 3;
+      const uint32_t slot = i & 3, par = i & 1, sb = i % 3;
       // control flow follows barrier reductions only, so the four warps agree
       bool ok = wait_bar(&itfull[slot], (i >> 2) & 1, limit, &abort_sh);
       const int item = ok ? it_sh[slot] : -1;
@@ -586,10 +650,20 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
       DecItem it;
       decode_item(p, item, it);
       const int R = p.group * it.Lq, nt = it.j1 - it.j0;
+      const int64_t first = (int64_t)p.item_off[it.s] + it.kvh;   // split qq is first + qq * Hkv
+      const int64_t bmo = p.bitmap ? p.bm_off[it.s] : 0;
       // key position of each row's query (rows past R: unused)
       int pos[RB];
 #pragma unroll
       for (int r = 0; r < RB; ++r) pos[r] = it.Lk - it.Lq + (r < R ? r % it.Lq : 0);
+      // the look-back's first window (the nearest 128 earlier splits): loads
+      // issued now, while this split's K tiles still stream in
+      uint64_t a[RB], c[RB];
+      if (t < it.q) {
+        const int64_t prow = (first + (int64_t)(it.q - 1 - t) * p.Hkv) * p.mpitch;
+        load_maxima<RB>(p.incl + prow, R, c);
+        load_maxima<RB>(p.agg + prow, R, a);
+      }
       ok = wait_bar(&sfull[sb], (i / 3) & 1, limit, &abort_sh);
       if (bar_red_or(!ok, 1, kGroup)) break;
       tc_fence_after();
@@ -614,88 +688,69 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
         for (int u = 0; u < nt; ++u)
           m = fmaxf(m, fmaxf(fmaxf(red[0][u * RB + t], red[1][u * RB + t]),
                              fmaxf(red[2][u * RB + t], red[3][u * RB + t])));
-        st_relaxed(p.agg + (int64_t)item * p.mpitch + t, publishable(m));
+        publish(p.agg + (int64_t)item * p.mpitch + t, p.epoch, m);
       }
-      named_bar_sync(1, kGroup);
-      if (t == 0) mbar_arrive(&mready[sb]);
-    }
-    if (abort_sh && t == 0) atomicExch(const_cast<int32_t *>(gabort), 1);
-  } else {
-    reg_alloc<kRegsPV>();
-    // ---------------------------------------------------- P V group
-    const int tp = t - kGroup, wp = warp - 4;   // key, head-dim column; warp in group
-    const uint32_t lane_off = (uint32_t)(wp * 32) << 16;
-    uint32_t kc = 0;
-    bool stop = false;
-    for (uint32_t i = 0; !stop; ++i) {
-      const uint32_t slot = i & 3, par = i & 1, sb = i % 3;
-      bool ok = wait_bar(&itfull[slot], (i >> 2) & 1, limit, &abort_sh);
-      const int item = ok ? it_sh[slot] : -1;
-      if (bar_red_or(!ok, 2, kGroup)) break;
-      if (tp == 0) mbar_arrive(&itempty[slot]);
-      if (item < 0) break;
-      DecItem it;
-      decode_item(p, item, it);
-      const int R = p.group * it.Lq, nt = it.j1 - it.j0;
-      const int64_t first = (int64_t)p.item_off[it.s] + it.kvh;   // split qq is first + qq * Hkv
-      const int64_t bmo = p.bitmap ? p.bm_off[it.s] : 0;
+      named_bar_sync(1, kGroup);   // tmax and the split maxima are out
 
-      // ---- running max before the split (while the score group still works
-      // on this split): nearest earlier splits first, 128 at a time, down to
-      // the nearest one with an inclusive prefix
+      // ---- running max before the split (after this split's own maxima are
+      // out, so that no split waits for one that waits for it): nearest
+      // earlier splits first, 128 at a time, down to the nearest one with an
+      // inclusive prefix; values the prefetch found unpublished are waited for
       float mp[RB];
 #pragma unroll
       for (int r = 0; r < RB; ++r) mp[r] = -INFINITY;
       bool fail = false, anyfail = false;
       for (int hi = it.q; hi > 0; hi -= kGroup) {
-        // thread tp: split qq; its row maxima (waited for) and, if every
+        // thread t: split qq; its row maxima (waited for) and, if every
         // row's inclusive prefix is out already, those
-        const int qq = hi - 1 - tp;
-        const bool mine = tp < hi;   // qq >= 0; the window is hi-128 .. hi-1
+        const int qq = hi - 1 - t;
+        const bool mine = t < hi;   // qq >= 0; the window is hi-128 .. hi-1
         const int64_t prow = (first + (int64_t)qq * p.Hkv) * p.mpitch;
-        float a[RB], c[RB];
         bool incl_ok = false;
         if (mine) {
-          load_maxima<RB>(p.incl + prow, R, c);
-          incl_ok = all_published<RB>(c, R);
-          if (!wait_maxima<RB>(p.agg + prow, R, a, limit, &abort_sh, gabort)) fail = true;
+          if (hi != it.q) {
+            load_maxima<RB>(p.incl + prow, R, c);
+            load_maxima<RB>(p.agg + prow, R, a);
+          }
+          incl_ok = all_published<RB>(c, R, p.epoch);
+          if (!all_published<RB>(a, R, p.epoch) &&
+              !wait_maxima<RB>(p.agg + prow, R, a, p.epoch, limit, &abort_sh, gabort))
+            fail = true;
         }
-        if (bar_red_or(fail, 2, kGroup)) {
+        if (bar_red_or(fail, 1, kGroup)) {
           anyfail = true;
           break;
         }
         const unsigned bal = __ballot_sync(0xffffffffu, incl_ok);
-        if (lane == 0) wmin[wp] = bal ? wp * 32 + __ffs(bal) - 1 : INT_MAX;
-        named_bar_sync(2, kGroup);
+        if (lane == 0) wmin[warp] = bal ? warp * 32 + __ffs(bal) - 1 : INT_MAX;
+        named_bar_sync(1, kGroup);
         const int tmin = min(min(wmin[0], wmin[1]), min(wmin[2], wmin[3]));
-        if (mine && tp <= tmin) {
+        if (mine && t <= tmin) {
 #pragma unroll
           for (int r = 0; r < RB; ++r)
-            if (r < R) mp[r] = fmaxf(mp[r], tp == tmin ? c[r] : a[r]);
+            if (r < R) mp[r] = fmaxf(mp[r], value_of(t == tmin ? c[r] : a[r]));
         }
-        named_bar_sync(2, kGroup);   // wmin is rewritten by the next window
+        named_bar_sync(1, kGroup);   // wmin is rewritten by the next window
         if (tmin != INT_MAX) break;
       }
       if (anyfail) {
-        stop = true;
+        abort_sh = 1;
         break;
       }
 #pragma unroll
       for (int r = 0; r < RB; ++r) {
         const float m = warp_max(mp[r]);
-        if (lane == 0) mred[wp][r] = m;
+        if (lane == 0) mred[warp][r] = m;
       }
-      // this split's tile maxima are in, and the kept lists of the item two
-      // back are no longer read
-      ok = wait_bar(&mready[sb], (i / 3) & 1, limit, &abort_sh) &&
-           wait_bar(&lfree[par], ((i >> 1) & 1) ^ 1, limit, &abort_sh);
-      if (bar_red_or(!ok, 2, kGroup)) break;
-      tc_fence_after();
+
+      // the kept lists of the item two back are no longer read
+      ok = wait_bar(&lfree[par], ((i >> 1) & 1) ^ 1, limit, &abort_sh);
+      if (bar_red_or(!ok, 1, kGroup)) break;
 
       // ---- decisions, in the group's first warp (R <= 32 rows): walk the
       // split's tiles in order per row; a head skips a tile when all its rows
       // do; the kept list and the skip bits follow from ballots
-      if (wp == 0) {
+      if (warp == 0) {
         uint32_t bits = 0;   // bit u: row lane would skip tile j0 + u
         if (lane < R) {
           float mr = fmaxf(fmaxf(mred[0][lane], mred[1][lane]), fmaxf(mred[2][lane], mred[3][lane]));
@@ -705,7 +760,7 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
             mr = fmaxf(mr, x);
           }
           // max over every tile up to the split's end: the later splits' look-back
-          st_relaxed(p.incl + (int64_t)item * p.mpitch + lane, publishable(mr));
+          publish(p.incl + (int64_t)item * p.mpitch + lane, p.epoch, mr);
         }
         // lane g < group: the tiles head g skips (the AND over its query rows)
         uint32_t hs = nt >= 32 ? 0xFFFFFFFFu : ((1u << nt) - 1u);
@@ -729,13 +784,43 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
           nkept_sh[par] = n;
           mbar_arrive(&lready[par]);
         }
-        if (p.bitmap && head && hs) {   // this split's bits of each head's row
+        if (p.bitmap && head) {   // this split's bits of each head's row: its range
+          // of the word cleared (the last split's reaches the word's end), then set
           const int nk = (it.Lk + kTile - 1) / kTile, W = (nk + 31) / 32;
-          atomicOr(p.bitmap + bmo + (int64_t)(it.kvh * p.group + lane) * W + (it.j0 >> 5),
-                   hs << (it.j0 & 31));
+          uint32_t *word = p.bitmap + bmo + (int64_t)(it.kvh * p.group + lane) * W + (it.j0 >> 5);
+          const uint32_t sh = it.j0 & 31;
+          const uint32_t range = it.q == it.ns - 1 ? 0xFFFFFFFFu << sh
+                                                   : (nt >= 32 ? 0xFFFFFFFFu : ((1u << nt) - 1u)) << sh;
+          atomicAnd(word, ~range);
+          if (hs) atomicOr(word, hs << sh);
         }
       }
-      named_bar_sync(2, kGroup);
+      named_bar_sync(1, kGroup);   // mred is rewritten by the next item
+    }
+    if (abort_sh && t == 0) atomicExch(const_cast<uint32_t *>(gabort), p.epoch);
+  } else {
+    reg_alloc<kRegsPV>();
+    // ---------------------------------------------------- P V group
+    const int tp = t - kGroup, wp = warp - 4;   // key, head-dim column; warp in group
+    const uint32_t lane_off = (uint32_t)(wp * 32) << 16;
+    uint32_t kc = 0;
+    bool stop = false;
+    for (uint32_t i = 0; !stop; ++i) {
+      const uint32_t slot = i & 3, par = i & 1, sb = i % 3;
+      bool ok = wait_bar(&itfull[slot], (i >> 2) & 1, limit, &abort_sh);
+      const int item = ok ? it_sh[slot] : -1;
+      if (bar_red_or(!ok, 2, kGroup)) break;
+      if (tp == 0) mbar_arrive(&itempty[slot]);
+      if (item < 0) break;
+      DecItem it;
+      decode_item(p, item, it);
+      const int R = p.group * it.Lq;
+      const int64_t first = (int64_t)p.item_off[it.s] + it.kvh;   // split qq is first + qq * Hkv
+
+      // the decisions of this split (the score group's)
+      ok = wait_bar(&lready[par], (i >> 1) & 1, limit, &abort_sh);
+      if (bar_red_or(!ok, 2, kGroup)) break;
+      tc_fence_after();
       const int n = nkept_sh[par];
 
       // ---- kept tiles
@@ -813,10 +898,14 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
       }
       if (!stop && n > 0 && !take_d(kc - 1)) stop = true;
       if (stop) break;
-      // the item's score columns are free for the item three ahead
+      // the item's score columns are free for the item three ahead, its kept
+      // list for the item two ahead
       tc_fence_before();
       named_bar_sync(2, kGroup);
-      if (tp == 0) mbar_arrive(&sfree[sb]);
+      if (tp == 0) {
+        mbar_arrive(&sfree[sb]);
+        mbar_arrive(&lfree[par]);
+      }
 
       // ---- partial result of the split (only if it kept a tile)
       if (n > 0) {
@@ -842,7 +931,7 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
       }
       named_bar_sync(2, kGroup);
       if (tp == 0) {   // the last of the splits of this (sequence, KV head) merges
-        if (n > 0) p.flags[item] = kFlagPart;
+        if (n > 0) p.flags[item] = p.epoch;
         merge_sh = atom_add_acq_rel(p.done + it.s * p.Hkv + it.kvh, 1) == it.ns - 1;
       }
       named_bar_sync(2, kGroup);
@@ -868,7 +957,7 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
       for (int b0 = 0; b0 < it.ns; b0 += kGroup) {
         const int qq = b0 + tp;
         const int64_t x = first + (int64_t)qq * p.Hkv;
-        const bool has = qq < it.ns && (__ldcg(p.flags + x) & kFlagPart);
+        const bool has = qq < it.ns && __ldcg(p.flags + x) == p.epoch;
         const unsigned bal = __ballot_sync(0xffffffffu, has);
         if (lane == 0) wcnt[wp] = __popc(bal);
         named_bar_sync(2, kGroup);
@@ -956,7 +1045,7 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
       named_bar_sync(2, kGroup);   // msh / lsh are reset by the next merge
     }
     if (stop) abort_sh = 1;
-    if (abort_sh && tp == 0) atomicExch(const_cast<int32_t *>(gabort), 1);
+    if (abort_sh && tp == 0) atomicExch(const_cast<uint32_t *>(gabort), p.epoch);
   }
   tc_fence_before();
   __syncthreads();
@@ -970,8 +1059,6 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
 cudaError_t launch_decode(const DecParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                           int sm_count, cudaStream_t stream) {
   const int grid = (int)(p.max_items < sm_count ? p.max_items : sm_count);
-  cudaError_t e = launch_dependent(dec_prologue_kernel, 1, 1024, 0, stream, p);
-  if (e != cudaSuccess) return e;
   if (p.rows <= 4)
     return launch_dependent(dec_kernel<4>, grid, kDecThreadsAll, DecCfg<4>::kSmem, stream, p, tk, tv);
   if (p.rows <= 8)

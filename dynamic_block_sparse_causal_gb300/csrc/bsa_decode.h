@@ -12,22 +12,27 @@ namespace bsa {
 
 constexpr int kDecMaxRows = 32;    // query rows per (sequence, KV head): group x Lq
 
-// Per-call counters of the decode kernel (zeroed by its prologue).
+// Per-call words of the decode kernel. Each call carries an epoch (a per
+// stream count of calls, never 0): per-call state is either written by the
+// call's set-up CTA before any item starts, or tagged with the epoch, so no
+// call has to clear what the one before left.
 struct alignas(128) DecWorkspace {
-  int32_t total_items;   // 0 when the arguments were rejected on the device
-  int32_t next_item;     // work-item counter the CTAs claim from
-  int32_t abort;         // set by a CTA that gave up a wait: the others stop
-  int32_t pad_[29];
+  int32_t total_items;   // set-up: work items (0 when the arguments were rejected)
+  int32_t next_item;     // set-up zeroes it; the CTAs claim work items from it
+  uint32_t abort;        // the epoch, once a CTA of that call gave up a wait
+  uint32_t setup_owner;  // the epoch, once a CTA of that call has taken the set-up
+  uint32_t setup_done;   // the epoch, once that call's tables are written
+  int32_t pad_[27];
 };
 
-// Per-stream scratch of the decode path. Tables follow the header:
-//   int32 item_off[n_seqs + 1]   first work item (KV head x split) of every sequence
-//   int64 bm_off[n_seqs + 1]     first skip-bitmap word of every sequence
-//   uint32 flags[items]          per work item: maxima / inclusive prefix
-//                                published, partial result written
-//   int32 done[n_seqs x Hkv]     finished work items per (sequence, KV head)
-//   float agg[items][mpitch]     the split's row maxima (log2 units)
-//   float incl[items][mpitch]    row maxima over every tile up to the split's end
+// Per-stream scratch of the decode path (zero-filled when allocated). Tables
+// follow the header:
+//   int32 item_off[n_seqs + 1]   set-up: first work item (KV head x split) of every sequence
+//   int64 bm_off[n_seqs + 1]     set-up: first skip-bitmap word of every sequence
+//   uint32 flags[items]          the epoch once the item's partial result is written
+//   int32 done[n_seqs x Hkv]     set-up zeroes them: finished items per (sequence, KV head)
+//   uint64 agg[items][mpitch]    (epoch << 32) | the split's row maxima (f32 bits, log2 units)
+//   uint64 incl[items][mpitch]   (epoch << 32) | row maxima over every tile up to the split's end
 //                                (mpitch = rows rounded up to a multiple of 4)
 //   float pO[items][rows][128], pm[items][rows], pl[items][rows]
 //                                per-split output, reference max, sum
@@ -51,9 +56,9 @@ struct DecLayout {
     off += up((size_t)n_seqs * Hkv * 4);
     const size_t mpitch = (size_t)(rows + 3) / 4 * 4;
     l.agg = off;
-    off += up((size_t)l.max_items * mpitch * 4);
+    off += up((size_t)l.max_items * mpitch * 8);
     l.incl = off;
-    off += up((size_t)l.max_items * mpitch * 4);
+    off += up((size_t)l.max_items * mpitch * 8);
     l.pO = off;
     off += up((size_t)l.max_items * rows * kTile * 4);
     l.pm = off;
@@ -74,7 +79,8 @@ struct DecParams {
   const int32_t *item_off;
   uint32_t *flags;
   int32_t *done;
-  float *agg, *incl, *pO, *pm, *pl;
+  uint64_t *agg, *incl;
+  float *pO, *pm, *pl;
   void *out;                  // bf16 [total_q, Hq, 128]
   float *lse;                 // [Hq, total_q] or null
   uint32_t *bitmap;           // or null
@@ -85,6 +91,7 @@ struct DecParams {
   int32_t split;              // key tiles per work item (decode_split(rows))
   float c, log2_lambda;
   uint64_t wait_limit_ns;
+  uint32_t epoch;             // this call's number on the stream (never 0)
   int32_t debug_drop_k_load;  // >= 0: the K producer omits that load (fault drill)
 };
 
