@@ -36,11 +36,12 @@
 // until it reads its own call's epoch. The first CTA to arrive writes the
 // call's tables (a block-wide scan over the sequences) while the others wait
 // for it; nothing else needs clearing between calls. An item waits only for
-// items of lower index; those were claimed earlier by CTAs that are running and publish
-// their maxima before they wait for anything outside their CTA, so the waits
-// end; each is bounded by the wait limit all the same. Decisions equal the sequential walk's; outputs equal
-// the online softmax over the kept tiles up to rounding order. The work is
-// bound by reading K once and the kept V once from DRAM.
+// items of lower index; those were claimed earlier by CTAs that are running
+// and publish their maxima before they wait for anything outside their CTA,
+// so the waits end; each is bounded by the wait limit all the same.
+// Decisions equal the sequential walk's; outputs equal the online softmax
+// over the kept tiles up to rounding order. The work is bound by reading K
+// once and the kept V once from DRAM.
 #include <cuda_bf16.h>
 
 #include <climits>
@@ -56,7 +57,6 @@ namespace {
 constexpr uint32_t kTileBytes = 32768;   // 128 keys x 128 bf16
 constexpr uint32_t kBoxBytes = 16384;    // one 128-row x 128-byte TMA box
 constexpr float kLn2 = 0.6931471805599453f;
-
 
 struct DecItem {
   int s, kvh, q, j0, j1, aq, Lq, ak, Lk, ns;
