@@ -263,9 +263,15 @@ int64_t bsa_skip_bitmap_words_chunked(const int32_t *cu_seqlens_q_host,
  *
  * The split restates the order rule: a skipped tile never raises the running
  * max (tile_max < m + ln(lambda) < m), so the running max before key tile j
- * is the prefix max of the tile maxima before j, and tile j's decision follows
- * from all tiles' maxima, computed first in parallel. Outputs are the online
- * softmax over the kept tiles, merged across splits (P and the merge in fp32).
+ * is the prefix max of the tile maxima before j. One persistent kernel (one
+ * CTA per SM) takes work items (sequence, KV head, split of 8 key tiles, or
+ * 4 when (Hq / Hkv) * max_seqlen_q > 16) in order: each publishes its split's
+ * tile maxima, reads those of the earlier splits of its (sequence, KV head),
+ * decides its tiles and computes P V for the kept ones; the split that
+ * finishes last merges the partial results. Outputs are the online softmax
+ * over the kept tiles, merged across splits (P and the merge in fp32). A
+ * work item waits (bounded by the wait limit) only for items of lower index;
+ * a wait that runs out stops the call and records BSA_ERR_TIMEOUT.
  *
  * q, k, v, cu_seqlens_q, cu_seqlens_k, n_seqs, Hq, Hkv, d, causal, lambda,
  * out, lse, skip_bitmap: as bsa_prefill_fwd_chunked (bfloat16 only; the bitmap
@@ -274,8 +280,10 @@ int64_t bsa_skip_bitmap_words_chunked(const int32_t *cu_seqlens_q_host,
  *               <= 32 and Hq / Hkv <= 16.
  * total_k       cu_seqlens_k[n_seqs], the rows of k and v (checked on the
  *               device; a mismatch writes nothing, BSA_ERR_BAD_SEQLENS).
- * Scratch (scores of the query rows for every key, per-split partial
- * outputs) is library-owned, per stream, grown stream-ordered.
+ * Scratch (per-split maxima, per-split partial outputs, per-call counters)
+ * is library-owned, per stream, grown stream-ordered and zero-filled when
+ * grown; per-call state carries a per-stream call count, so a call that
+ * stopped early leaves nothing the next one has to clear.
  */
 bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
                             const int32_t *cu_seqlens_q,

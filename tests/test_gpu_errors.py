@@ -63,7 +63,7 @@ def _drill_args(p):
 
 
 def test_fault_drill_in_decode_and_importance():
-    """The same drill in the split-KV decode score kernel and the importance
+    """The same drill in the split-KV decode kernel and the importance
     score kernel: each CTA's first K load is left out, the call records
     BSA_ERR_TIMEOUT, and the next normal calls are correct."""
     import test_gpu_decode as td

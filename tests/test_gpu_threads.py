@@ -91,3 +91,79 @@ def test_two_threads_two_streams_match_single_calls_and_oracle():
                           streams[0]), "after release")
     torch.cuda.synchronize()
     assert torch.equal(out, refs[0]["out"])
+
+
+def test_two_threads_two_streams_decode():
+    """Decode calls from two host threads on two streams: two persistent
+    decode grids may share the GPU. Each grid's work items wait only for items
+    its own running CTAs claimed, so both finish; every result equals, bit for
+    bit, the same call made alone (which matches the oracle), and a released
+    stream's scratch is rebuilt (zero-filled) on its next call."""
+    import test_gpu_decode as td
+    from gen import inputs as gi
+    b = _gpu.bsa()
+    bases = [gi.packed("dec2a", [20000, 9000], Hq=8, Hkv=2, seed=5, window=2.0,
+                       window_period=4096, window_len=512),
+             gi.packed("dec2b", [30000], Hq=16, Hkv=2, seed=6, window=2.0, window_period=4096,
+                       window_len=512)]
+    probs = [gi.chunk(bases[0], [1, 2]), gi.chunk(bases[1], [3])]
+    refs = []
+    for p in probs:
+        g, st = td.run_decode(p, 0.005)
+        assert st == 0
+        _gpu.compare(p, g)
+        refs.append(g)
+    n_calls = 6
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    ins, outs = [], []
+    for p in probs:
+        q, k, v = _gpu.to_dev_bf16(p.q), _gpu.to_dev_bf16(p.k), _gpu.to_dev_bf16(p.v)
+        cq = torch.from_numpy(p.cu_seqlens.astype(np.int32)).cuda()
+        ck = torch.from_numpy(p.cu_seqlens_k.astype(np.int32)).cuda()
+        ins.append((q, k, v, cq, ck))
+        nw = b.skip_bitmap_words_chunked(p.cu_seqlens, p.cu_seqlens_k, p.Hq)
+        outs.append([(torch.empty((p.total_tokens, p.Hq, p.d), dtype=torch.bfloat16, device="cuda"),
+                      torch.empty((p.Hq, p.total_tokens), dtype=torch.float32, device="cuda"),
+                      torch.full((nw,), -1, dtype=torch.int32, device="cuda")) for _ in range(n_calls)])
+    torch.cuda.synchronize()
+    errors = []
+    start = threading.Barrier(2)
+
+    def call(t, n, stream):
+        p = probs[t]
+        q, k, v, cq, ck = ins[t]
+        out, lse, bm = outs[t][n]
+        return b.decode_fwd(q, k, v, cq, ck, p.n_seqs, int(p.seqlens.max()), int(p.cu_seqlens_k[-1]),
+                            p.Hq, p.Hkv, p.d, 1, 0.005, out, lse, bm, stream)
+
+    def worker(t):
+        try:
+            torch.cuda.set_device(0)
+            start.wait()
+            for n in range(n_calls):
+                st = call(t, n, streams[t])
+                if st != 0:
+                    errors.append((t, n, st))
+        except Exception as e:  # reported below
+            errors.append((t, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for t in range(2):
+        assert b.get_device_status(streams[t]) == 0
+        for out, lse, bm in outs[t]:
+            assert torch.equal(out, refs[t]["out"]) and torch.equal(lse, refs[t]["lse"])
+            assert np.array_equal(bm.cpu().numpy().view(np.uint32), refs[t]["bitmap"])
+    assert b.release_stream(streams[0]) == 0
+    torch.cuda.synchronize()
+    out, lse, bm = outs[0][0]
+    out.fill_(float("nan"))
+    b.check(call(0, 0, streams[0]), "after release")
+    torch.cuda.synchronize()
+    assert torch.equal(out, refs[0]["out"])
+    assert np.array_equal(bm.cpu().numpy().view(np.uint32), refs[0]["bitmap"])
