@@ -927,8 +927,12 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
           for (int r = 0; r < RB; ++r)
             if (r == tp) p.pm[prow + tp] = mref[r];
         }
-        __threadfence();   // the partial is visible before the count below
       }
+      // The group's writes of the partial result are ordered before thread
+      // 0's count by the barrier, and the count (acq_rel, gpu scope) releases
+      // them with it: the CTA whose count completes the (sequence, KV head)
+      // acquires every earlier count's writes, and its barrier hands them to
+      // its whole group, which reads them from L2.
       named_bar_sync(2, kGroup);
       if (tp == 0) {   // the last of the splits of this (sequence, KV head) merges
         if (n > 0) p.flags[item] = p.epoch;
@@ -936,7 +940,6 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
       }
       named_bar_sync(2, kGroup);
       if (!merge_sh) continue;
-      __threadfence();
 
       // ---- merge: the splits of this (sequence, KV head) that kept a tile,
       // in split order: 128 candidates at a time, their list taken in batches
