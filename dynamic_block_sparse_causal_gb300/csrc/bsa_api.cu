@@ -43,6 +43,7 @@ struct StreamState {
   std::mutex mu;
   Buffer ws, imp, dec;
   uint32_t dec_epoch = 0;   // decode calls on this stream (tags their per-call state)
+  bsa::DecCaps dec_caps;    // sizes the decode tables are laid out for
 };
 
 std::mutex g_mu;   // guards g_streams, g_devices and g_encode
@@ -327,17 +328,25 @@ bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
   if ((st = scratch_for(ss, stream, sizeof(Workspace), &ws)) != BSA_OK) return st;
   const int rows = group * max_seqlen_q;
   const int split = bsa::decode_split(rows);
-  const bsa::DecLayout layout = bsa::DecLayout::make(n_seqs, Hkv, rows, total_k, split);
+  bsa::DecCaps need;
+  need.n_seqs = n_seqs;
+  need.seq_heads = (int64_t)n_seqs * Hkv;
+  need.rows = rows;
+  need.items = (int64_t)Hkv * ((total_k / bsa::kTile + n_seqs) / split + n_seqs);
+  // the tables keep their layout while it covers the call; a new layout (or a
+  // new buffer, or the count of calls wrapping) starts from zeroes
+  bool reset = !ss->dec_caps.covers(need);
+  if (reset) ss->dec_caps = ss->dec_caps.grown_to(need);
+  const bsa::DecLayout layout = bsa::DecLayout::make(ss->dec_caps);
   void *buf = nullptr;
   bool grown = false;
   if ((st = table_for(ss->dec, stream, layout.bytes, &buf, &grown)) != BSA_OK) return st;
-  // epoch-tagged state: a new buffer starts at zero (no epoch), and so does
-  // the buffer once the count of calls wraps
   if (++ss->dec_epoch == 0) {
     ss->dec_epoch = 1;
-    grown = true;
+    reset = true;
   }
-  if (grown && cudaMemsetAsync(buf, 0, ss->dec.bytes, stream) != cudaSuccess) return BSA_ERR_CUDA;
+  if ((reset || grown) && cudaMemsetAsync(buf, 0, ss->dec.bytes, stream) != cudaSuccess)
+    return BSA_ERR_CUDA;
   char *base = static_cast<char *>(buf);
   bsa::DecParams p{};
   p.dw = static_cast<bsa::DecWorkspace *>(buf);
@@ -349,7 +358,7 @@ bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
   p.item_off = reinterpret_cast<const int32_t *>(base + layout.item_off);
   p.bm_off = reinterpret_cast<const int64_t *>(base + layout.bm_off);
   p.flags = reinterpret_cast<uint32_t *>(base + layout.flags);
-  p.done = reinterpret_cast<int32_t *>(base + layout.done);
+  p.done = reinterpret_cast<uint64_t *>(base + layout.done);
   p.agg = reinterpret_cast<uint64_t *>(base + layout.agg);
   p.incl = reinterpret_cast<uint64_t *>(base + layout.incl);
   p.pO = reinterpret_cast<float *>(base + layout.pO);
@@ -359,13 +368,13 @@ bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
   p.lse = lse;
   p.bitmap = skip_bitmap;
   p.total_k = total_k;
-  p.max_items = layout.max_items;
+  p.max_items = need.items;
   p.n_seqs = n_seqs;
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.group = group;
   p.rows = rows;
-  p.mpitch = (rows + 3) / 4 * 4;
+  p.mpitch = (int32_t)layout.mpitch;
   p.max_q = max_seqlen_q;
   p.split = split;
   p.causal = causal;

@@ -62,11 +62,13 @@ struct DecItem {
   int s, kvh, q, j0, j1, aq, Lq, ak, Lk, ns;
 };
 
-__device__ __forceinline__ void decode_item(const DecParams &p, int item, DecItem &it) {
+// item_off: the call's per-sequence first work items (shared memory or scratch)
+__device__ __forceinline__ void decode_item(const DecParams &p, const int32_t *item_off, int item,
+                                            DecItem &it) {
   int lo = 0, hi = p.n_seqs;   // largest s with item_off[s] <= item
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (p.item_off[mid] <= item) lo = mid; else hi = mid;
+    if (item_off[mid] <= item) lo = mid; else hi = mid;
   }
   it.s = lo;
   it.aq = p.cu_q[lo];
@@ -77,7 +79,7 @@ __device__ __forceinline__ void decode_item(const DecParams &p, int item, DecIte
   it.ns = (nk + p.split - 1) / p.split;
   // the KV heads of one split are neighbours: CTAs running together read
   // whole token rows of K and V (all heads) from DRAM
-  const int local = item - p.item_off[lo];
+  const int local = item - item_off[lo];
   it.q = local / p.Hkv;
   it.kvh = local - it.q * p.Hkv;
   it.j0 = it.q * p.split;
@@ -111,10 +113,22 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *a) {
 __device__ __forceinline__ void st_release_u32(uint32_t *a, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
 }
-__device__ __forceinline__ int atom_add_acq_rel(int32_t *a, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
-  return old;
+// Epoch-tagged counters (epoch << 32 | count): lift a word an earlier call
+// left to (epoch, 0) -- epochs only grow -- then count; same thread, same
+// word, so the add sees the lift.
+__device__ __forceinline__ void counter_enter(uint64_t *a, uint32_t epoch) {
+  asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(a), "l"((uint64_t)epoch << 32)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t counter_add(uint64_t *a) {
+  uint64_t old;
+  asm volatile("atom.relaxed.gpu.global.add.u64 %0, [%1], 1;" : "=l"(old) : "l"(a) : "memory");
+  return (uint32_t)old;
+}
+__device__ __forceinline__ uint32_t counter_add_acq_rel(uint64_t *a) {
+  uint64_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], 1;" : "=l"(old) : "l"(a) : "memory");
+  return (uint32_t)old;
 }
 
 // Wait for a phase of an mbarrier; false when the CTA is aborting or the wait
@@ -247,21 +261,18 @@ constexpr int kMaxSplitRB = 128;     // kSplit x RB: tile-max entries of one ite
 
 }  // namespace
 
-// The call's tables, written by all threads of the first CTA to arrive: per
-// sequence its first work item and first skip-bitmap word (a block-wide scan
-// over the sequences, NT at a time), the checks of the lengths on the
-// device, the item count, and the zeroed counters.
+// The call's tables, written by all NT threads of a CTA: per sequence its
+// first work item and first skip-bitmap word (a block-wide scan over the
+// sequences, NT at a time) into item_off / bm_off, the checks of the lengths
+// on the device, and the item count into items_sh (0 when rejected).
+// bad_sh and carry start at zero (set with the barriers at kernel start), so
+// the first loads of the lengths are also the first memory round trip.
 template <int NT>
-__device__ void dec_setup(const DecParams &p, long long (&wsum)[NT / 32][2], long long (&carry)[2],
-                          int &bad_sh) {
+__device__ void dec_tables(const DecParams &p, long long (&wsum)[NT / 32][2], long long (&carry)[2],
+                           int &bad_sh, int32_t *item_off, int64_t *bm_off, int &items_sh) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  if (t == 0) {
-    bad_sh = p.cu_q[0] != 0 || p.cu_k[0] != 0 || (int64_t)p.cu_k[p.n_seqs] != p.total_k;
-    carry[0] = carry[1] = 0;
-  }
-  __syncthreads();
-  int32_t *item_off = const_cast<int32_t *>(p.item_off);
-  int64_t *bm_off = const_cast<int64_t *>(p.bm_off);
+  if (t == 0 && (p.cu_q[0] != 0 || p.cu_k[0] != 0 || (int64_t)p.cu_k[p.n_seqs] != p.total_k))
+    atomicOr(&bad_sh, 1);
   for (int b0 = 0; b0 < p.n_seqs; b0 += NT) {
     const int s = b0 + t;
     long long ni = 0, nw = 0;   // this sequence's work items and bitmap words
@@ -312,11 +323,9 @@ __device__ void dec_setup(const DecParams &p, long long (&wsum)[NT / 32][2], lon
     item_off[p.n_seqs] = (int32_t)min(items, (long long)INT_MAX);
     bm_off[p.n_seqs] = carry[1];
     const bool bad = bad_sh != 0 || items > p.max_items;
-    p.dw->total_items = bad ? 0 : (int32_t)items;
-    p.dw->next_item = 0;
+    items_sh = bad ? 0 : (int32_t)items;
     if (bad) atomicOr(&p.ws->status, kStatusBadSeqlens);
   }
-  for (int x = t; x < p.n_seqs * p.Hkv; x += NT) p.done[x] = 0;
   __syncthreads();
 }
 
@@ -358,7 +367,9 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
       qready[2], qfree[2], sfull[3], sfree[3], lready[2], lfree[2], pready[2], pfree[2],
       dfull[2], dempty[2], drain[2];
   __shared__ long long wsum[kDecThreadsAll / 32][2], carry[2];
-  __shared__ int bad_sh, owner_sh;
+  __shared__ int bad_sh, owner_sh, items_sh;
+  __shared__ int32_t s_iofs[kDecLocalSeqs + 1];
+  __shared__ int64_t s_bofs[kDecLocalSeqs + 1];
   __shared__ uint32_t tmem_sh;
   __shared__ volatile int abort_sh;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -395,6 +406,8 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
     }
     fence_mbar_init();
     abort_sh = 0;
+    bad_sh = 0;
+    carry[0] = carry[1] = 0;
   }
   if (warp == 10) {
     tmem_alloc(&tmem_sh, 512);
@@ -412,26 +425,44 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
   grid_dep_launch();
   const uint64_t limit = p.wait_limit_ns;
   const volatile uint32_t *gabort = &p.dw->abort;   // == epoch: a CTA gave up
-  // the call's tables: the first CTA to arrive writes them, the others wait
-  if (t == 0) owner_sh = atomicExch(&p.dw->setup_owner, p.epoch) != p.epoch;
-  __syncthreads();
-  if (owner_sh) {
-    dec_setup<kDecThreadsAll>(p, wsum, carry, bad_sh);
-    if (t == 0) {
-      __threadfence();
-      st_release_u32(&p.dw->setup_done, p.epoch);
+  // the first claim goes out now: its round trip overlaps the tables
+  uint32_t first_claim = 0;
+  if (warp == 8 && lane == 0) {
+    counter_enter(&p.dw->claim, p.epoch);
+    first_claim = counter_add(&p.dw->claim);
+  }
+  // the call's tables: a batch of at most kDecLocalSeqs sequences in every
+  // CTA's shared memory; a larger one once, by the first CTA to arrive, in the
+  // scratch, while the others wait for it
+  const bool local_tables = p.n_seqs <= kDecLocalSeqs;
+  if (local_tables) {
+    dec_tables<kDecThreadsAll>(p, wsum, carry, bad_sh, s_iofs, s_bofs, items_sh);
+  } else {
+    if (t == 0) owner_sh = atomicExch(&p.dw->setup_owner, p.epoch) != p.epoch;
+    __syncthreads();
+    if (owner_sh) {
+      dec_tables<kDecThreadsAll>(p, wsum, carry, bad_sh, const_cast<int32_t *>(p.item_off),
+                                 const_cast<int64_t *>(p.bm_off), items_sh);
+      if (t == 0) {
+        p.dw->total_items = items_sh;
+        __threadfence();
+        st_release_u32(&p.dw->setup_done, p.epoch);
+      }
+    } else if (t == 0) {
+      bool ok = ld_acquire_u32(&p.dw->setup_done) == p.epoch;
+      const uint64_t t0 = globaltimer_ns();
+      while (!ok && globaltimer_ns() - t0 <= limit) {
+        __nanosleep(100);
+        ok = ld_acquire_u32(&p.dw->setup_done) == p.epoch;
+      }
+      items_sh = ok ? __ldcg(&p.dw->total_items) : 0;
+      if (!ok) abort_sh = 1;
     }
-  } else if (t == 0) {
-    bool ok = ld_acquire_u32(&p.dw->setup_done) == p.epoch;
-    const uint64_t t0 = globaltimer_ns();
-    while (!ok && globaltimer_ns() - t0 <= limit) {
-      __nanosleep(100);
-      ok = ld_acquire_u32(&p.dw->setup_done) == p.epoch;
-    }
-    if (!ok) abort_sh = 1;
   }
   __syncthreads();
-  const int total = abort_sh ? 0 : __ldcg(&p.dw->total_items);
+  const int total = abort_sh ? 0 : items_sh;
+  const int32_t *iofs = local_tables ? s_iofs : p.item_off;
+  const int64_t *bofs = local_tables ? s_bofs : p.bm_off;
 
   if (warp >= 8) {
     reg_dealloc<kRegsIssue>();
@@ -452,8 +483,8 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
           // claims only (never a fixed item per CTA): every claimed item then
           // belongs to a CTA that is running, even when other grids hold SMs
           if (ok && !abort_sh && *gabort != p.epoch) {
-            item = atomicAdd(&p.dw->next_item, 1);
-            if (item >= total) item = -1;
+            const uint32_t c = i == 0 ? first_claim : counter_add(&p.dw->claim);
+            item = c >= (uint32_t)total ? -1 : (int)c;
           }
           if (ok) {
             it_sh[slot] = item;
@@ -466,7 +497,7 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
         item = __shfl_sync(0xffffffffu, item, 0);
         if (!ok || item < 0) break;
         DecItem it;
-        decode_item(p, item, it);
+        decode_item(p, iofs, item, it);
         // K loads into ring stages that are free right now go first (at the
         // start, the whole ring), the rest after the query rows are staged
         int jn = it.j0;
@@ -525,7 +556,7 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
           mbar_arrive(&itempty[slot]);
           if (item < 0) break;
           DecItem it;
-          decode_item(p, item, it);
+          decode_item(p, iofs, item, it);
           if (!wait_bar(&lready[par], (i >> 1) & 1, limit, &abort_sh)) break;
           const int n = nkept_sh[par];
           // every kept tile's V heads for L2 at once; the two ring stages then
@@ -560,7 +591,7 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
           mbar_arrive(&itempty[slot]);
           if (item < 0) break;
           DecItem it;
-          decode_item(p, item, it);
+          decode_item(p, iofs, item, it);
           // the query rows are staged, and the P V group is done with the S
           // columns of the item three back
           const uint32_t sb = i % 3;
@@ -648,10 +679,10 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
       if (t == 0) mbar_arrive(&itempty[slot]);
       if (item < 0) break;
       DecItem it;
-      decode_item(p, item, it);
+      decode_item(p, iofs, item, it);
       const int R = p.group * it.Lq, nt = it.j1 - it.j0;
-      const int64_t first = (int64_t)p.item_off[it.s] + it.kvh;   // split qq is first + qq * Hkv
-      const int64_t bmo = p.bitmap ? p.bm_off[it.s] : 0;
+      const int64_t first = (int64_t)iofs[it.s] + it.kvh;   // split qq is first + qq * Hkv
+      const int64_t bmo = p.bitmap ? bofs[it.s] : 0;
       // key position of each row's query (rows past R: unused)
       int pos[RB];
 #pragma unroll
@@ -813,9 +844,9 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
       if (tp == 0) mbar_arrive(&itempty[slot]);
       if (item < 0) break;
       DecItem it;
-      decode_item(p, item, it);
+      decode_item(p, iofs, item, it);
       const int R = p.group * it.Lq;
-      const int64_t first = (int64_t)p.item_off[it.s] + it.kvh;   // split qq is first + qq * Hkv
+      const int64_t first = (int64_t)iofs[it.s] + it.kvh;   // split qq is first + qq * Hkv
 
       // the decisions of this split (the score group's)
       ok = wait_bar(&lready[par], (i >> 1) & 1, limit, &abort_sh);
@@ -936,7 +967,9 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
       named_bar_sync(2, kGroup);
       if (tp == 0) {   // the last of the splits of this (sequence, KV head) merges
         if (n > 0) p.flags[item] = p.epoch;
-        merge_sh = atom_add_acq_rel(p.done + it.s * p.Hkv + it.kvh, 1) == it.ns - 1;
+        uint64_t *done = p.done + it.s * p.Hkv + it.kvh;
+        counter_enter(done, p.epoch);
+        merge_sh = counter_add_acq_rel(done) == (uint32_t)(it.ns - 1);
       }
       named_bar_sync(2, kGroup);
       if (!merge_sh) continue;

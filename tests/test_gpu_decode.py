@@ -148,3 +148,65 @@ def test_decode_rejects_bad_lengths():
     g, st = run_decode(p, 0.005, total_k=int(p.cu_seqlens_k[-1]) - 1, fill=7.0)
     assert st == 6 and bool((g["out"] == 7.0).all())
     assert b.get_device_status() == 0
+
+
+def test_decode_tables_reused_across_shapes():
+    """One stream alternates a small and a larger decode problem: the scratch
+    is laid out again (and cleared) when a call needs more room, and reused,
+    with per-call state told apart by the call count, otherwise. Every call
+    equals, bit for bit, the same call on a fresh stream."""
+    b = _gpu.bsa()
+    small = gi.chunk(_cases.small_problem("gqa_ragged"), [1, 2, 1, 1])
+    big = gi.chunk(gi.packed("decbig", [9000, 5000, 7000], Hq=8, Hkv=2, seed=8, window=2.0,
+                             window_period=4096, window_len=512), [4, 1, 2])
+    probs = [small, big]
+    ins = []
+    for p in probs:
+        ins.append((_gpu.to_dev_bf16(p.q), _gpu.to_dev_bf16(p.k), _gpu.to_dev_bf16(p.v),
+                    torch.from_numpy(p.cu_seqlens.astype(np.int32)).cuda(),
+                    torch.from_numpy(p.cu_seqlens_k.astype(np.int32)).cuda()))
+
+    def call(t, stream):
+        p = probs[t]
+        q, k, v, cq, ck = ins[t]
+        out = torch.full((p.total_tokens, p.Hq, p.d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((p.Hq, p.total_tokens), float("nan"), dtype=torch.float32, device="cuda")
+        nw = b.skip_bitmap_words_chunked(p.cu_seqlens, p.cu_seqlens_k, p.Hq)
+        bm = torch.full((nw,), -1, dtype=torch.int32, device="cuda")
+        b.check(b.decode_fwd(q, k, v, cq, ck, p.n_seqs, int(p.seqlens.max()), int(p.cu_seqlens_k[-1]),
+                             p.Hq, p.Hkv, p.d, 1, 0.005, out, lse, bm, stream), "decode")
+        return out, lse, bm
+
+    refs = []
+    for t in range(2):
+        s = torch.cuda.Stream()
+        refs.append(call(t, s))
+        torch.cuda.synchronize()
+        assert b.get_device_status(s) == 0
+        assert b.release_stream(s) == 0
+    s = torch.cuda.Stream()
+    for t in (0, 1, 0, 0, 1, 1, 0):
+        out, lse, bm = call(t, s)
+        torch.cuda.synchronize()
+        assert b.get_device_status(s) == 0
+        assert torch.equal(out, refs[t][0]) and torch.equal(lse, refs[t][1])
+        assert torch.equal(bm, refs[t][2])
+    assert b.release_stream(s) == 0
+    g, st = run_decode(big, 0.005)
+    assert st == 0
+    _gpu.compare(big, g)
+
+
+def test_decode_batch_above_local_table_size():
+    """300 sequences (more than the 256 whose tables every CTA builds for
+    itself): one CTA writes the per-sequence tables and the others wait for
+    it. Mixed lengths (1 to 1100 keys), one or two new queries each."""
+    rng = np.random.default_rng(11)
+    lens = [int(x) for x in rng.integers(2, 1100, 300)]
+    base = gi.packed("dec300", lens, Hq=8, Hkv=2, seed=12)
+    lq = [1 + (i % 2) for i in range(300)]
+    p = gi.chunk(base, lq)
+    for lam in (0.005, 0.0):
+        g, st = run_decode(p, lam)
+        assert st == 0
+        print(lam, _gpu.compare(p, g))
