@@ -281,9 +281,10 @@ int64_t bsa_skip_bitmap_words_chunked(const int32_t *cu_seqlens_q_host,
  * total_k       cu_seqlens_k[n_seqs], the rows of k and v (checked on the
  *               device; a mismatch writes nothing, BSA_ERR_BAD_SEQLENS).
  * Scratch (per-split maxima, per-split partial outputs, per-call counters)
- * is library-owned, per stream, grown stream-ordered and zero-filled when
- * grown; per-call state carries a per-stream call count, so a call that
- * stopped early leaves nothing the next one has to clear.
+ * is library-owned, per stream, grown stream-ordered, laid out for sizes that
+ * only grow and zero-filled whenever it is laid out again; per-call state
+ * carries a per-stream call count, so a call that stopped early leaves
+ * nothing the next one has to clear.
  */
 bsa_status_t bsa_decode_fwd(const void *q, const void *k, const void *v,
                             const int32_t *cu_seqlens_q,
