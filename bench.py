@@ -505,6 +505,88 @@ def gpu_arm(args, rank, world, local_rank):
                 "frac_per_clock": round((achieved / clocks["sm_mhz"]) /
                                         (peaks["bf16_tflops_sustained"] / pk), 4)}
 
+    # end to end through the C interface with host buffers: every step copies
+    # its inputs in from pinned host memory and its results (out, lse, skip
+    # bitmap) back out. Two device buffer sets and two host result sets let
+    # step i + 1's upload and step i - 1's download run on copy streams while
+    # step i computes; the timed region includes the first upload and the
+    # last download. The same steps run back to back on one stream are
+    # reported beside it. Measured right after the resident steps, so that
+    # both run in the same state of the GPU (the other legs heat it).
+    e2e = None
+    if not args.no_e2e:
+        hq = torch.from_numpy(p.q.view(np.int16)).pin_memory()
+        hk = torch.from_numpy(p.k.view(np.int16)).pin_memory()
+        hv = torch.from_numpy(p.v.view(np.int16)).pin_memory()
+        hcu = torch.from_numpy(p.cu_seqlens).pin_memory()
+        hres = [(torch.empty((T, Hq, d), dtype=torch.int16).pin_memory(),
+                 torch.empty((Hq, T), dtype=torch.float32).pin_memory(),
+                 torch.empty((nw,), dtype=torch.int32).pin_memory()) for _ in range(2)]
+        dbuf = [(q, k, v, cu, out, lse, bm),
+                (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(cu),
+                 torch.empty_like(out), torch.empty_like(lse), torch.empty_like(bm))]
+        s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev = {n: [torch.cuda.Event(), torch.cuda.Event()] for n in ("up", "comp", "down")}
+        used = [False, False]
+
+        def e2e_step(i, overlap=True):
+            bi = i % 2 if overlap else 0
+            dq, dk, dv, dcu, dout, dlse, dbm = dbuf[bi]
+            ho, hl, hb = hres[bi]
+            s_in = s_up if overlap else stream
+            s_out = s_down if overlap else stream
+            with torch.cuda.stream(s_in):
+                if used[bi]:
+                    s_in.wait_event(ev["comp"][bi])       # the forward that last read this set
+                dq.view(torch.int16).copy_(hq, non_blocking=True)
+                dk.view(torch.int16).copy_(hk, non_blocking=True)
+                dv.view(torch.int16).copy_(hv, non_blocking=True)
+                dcu.copy_(hcu, non_blocking=True)
+                ev["up"][bi].record(s_in)
+            stream.wait_event(ev["up"][bi])
+            if used[bi]:
+                stream.wait_event(ev["down"][bi])         # the download that last read out / lse / bitmap
+            st = bsa.prefill_fwd(dq, dk, dv, dcu, p.n_seqs, Hq, Hkv, d, 1, args.lam, bsa.BSA_BF16,
+                                 dout, dlse, dbm, stream)
+            if st != 0:
+                raise bsa.BsaError(st, "bsa_prefill_fwd")
+            ev["comp"][bi].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev["comp"][bi])
+                ho.copy_(dout.view(torch.int16), non_blocking=True)
+                hl.copy_(dlse, non_blocking=True)
+                hb.copy_(dbm, non_blocking=True)
+                ev["down"][bi].record(s_out)
+            used[bi] = True
+
+        def run_e2e(n, overlap):
+            for i in range(2):
+                e2e_step(i, overlap)
+            torch.cuda.synchronize()
+            barrier(world)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for i in range(n):
+                e2e_step(i, overlap)
+            torch.cuda.synchronize()
+            barrier(world)
+            return max_over_ranks((time.perf_counter() - t0) * 1e3 / n, world, dev)
+
+        n_e2e = max(4, args.steps)   # the first upload and last download amortise over these
+        ms_e2e = run_e2e(n_e2e, True)
+        ms_serial = run_e2e(max(2, args.steps // 2), False)
+        h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + hcu.numel() * 4
+        d2h = hres[0][0].numel() * 2 + hres[0][1].numel() * 4 + hres[0][2].numel() * 4
+        e2e = {"value": round(job_flops / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "ms_per_step": round(ms_e2e, 3), "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
+               "overlap": "upload of step i+1 and download of step i-1 on copy streams during the "
+                          "forward of step i (two buffer sets); first upload and last download timed",
+               "serial_ms_per_step": round(ms_serial, 3),
+               "serial_value": round(job_flops / (ms_serial * 1e-3) / 1e12, 2)}
+        bsa.check(bsa.get_device_status(stream), "device status")
+        del dbuf, hres
+
     # lambda sweep on the same layer (skip fraction and TFLOP/s for each lambda)
     sweep = []
     if not args.no_sweep:
@@ -727,87 +809,6 @@ def gpu_arm(args, rank, world, local_rank):
     dense_ref = None
     if not args.no_sweep and p.n_seqs == 1:
         dense_ref = sdpa_backends(q, k, v, T, Hq, Hkv, d, dflops, peak, args.steps, stream)
-
-    # end to end through the C interface with host buffers: every step copies
-    # its inputs in from pinned host memory and its results (out, lse, skip
-    # bitmap) back out. Two device buffer sets and two host result sets let
-    # step i + 1's upload and step i - 1's download run on copy streams while
-    # step i computes; the timed region includes the first upload and the
-    # last download. The same steps run back to back on one stream are
-    # reported beside it.
-    e2e = None
-    if not args.no_e2e:
-        hq = torch.from_numpy(p.q.view(np.int16)).pin_memory()
-        hk = torch.from_numpy(p.k.view(np.int16)).pin_memory()
-        hv = torch.from_numpy(p.v.view(np.int16)).pin_memory()
-        hcu = torch.from_numpy(p.cu_seqlens).pin_memory()
-        hres = [(torch.empty((T, Hq, d), dtype=torch.int16).pin_memory(),
-                 torch.empty((Hq, T), dtype=torch.float32).pin_memory(),
-                 torch.empty((nw,), dtype=torch.int32).pin_memory()) for _ in range(2)]
-        dbuf = [(q, k, v, cu, out, lse, bm),
-                (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(cu),
-                 torch.empty_like(out), torch.empty_like(lse), torch.empty_like(bm))]
-        s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        ev = {n: [torch.cuda.Event(), torch.cuda.Event()] for n in ("up", "comp", "down")}
-        used = [False, False]
-
-        def e2e_step(i, overlap=True):
-            bi = i % 2 if overlap else 0
-            dq, dk, dv, dcu, dout, dlse, dbm = dbuf[bi]
-            ho, hl, hb = hres[bi]
-            s_in = s_up if overlap else stream
-            s_out = s_down if overlap else stream
-            with torch.cuda.stream(s_in):
-                if used[bi]:
-                    s_in.wait_event(ev["comp"][bi])       # the forward that last read this set
-                dq.view(torch.int16).copy_(hq, non_blocking=True)
-                dk.view(torch.int16).copy_(hk, non_blocking=True)
-                dv.view(torch.int16).copy_(hv, non_blocking=True)
-                dcu.copy_(hcu, non_blocking=True)
-                ev["up"][bi].record(s_in)
-            stream.wait_event(ev["up"][bi])
-            if used[bi]:
-                stream.wait_event(ev["down"][bi])         # the download that last read out / lse / bitmap
-            st = bsa.prefill_fwd(dq, dk, dv, dcu, p.n_seqs, Hq, Hkv, d, 1, args.lam, bsa.BSA_BF16,
-                                 dout, dlse, dbm, stream)
-            if st != 0:
-                raise bsa.BsaError(st, "bsa_prefill_fwd")
-            ev["comp"][bi].record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev["comp"][bi])
-                ho.copy_(dout.view(torch.int16), non_blocking=True)
-                hl.copy_(dlse, non_blocking=True)
-                hb.copy_(dbm, non_blocking=True)
-                ev["down"][bi].record(s_out)
-            used[bi] = True
-
-        def run_e2e(n, overlap):
-            for i in range(2):
-                e2e_step(i, overlap)
-            torch.cuda.synchronize()
-            barrier(world)
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            for i in range(n):
-                e2e_step(i, overlap)
-            torch.cuda.synchronize()
-            barrier(world)
-            return max_over_ranks((time.perf_counter() - t0) * 1e3 / n, world, dev)
-
-        n_e2e = max(4, args.steps)   # the first upload and last download amortise over these
-        ms_e2e = run_e2e(n_e2e, True)
-        ms_serial = run_e2e(max(2, args.steps // 2), False)
-        h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + hcu.numel() * 4
-        d2h = hres[0][0].numel() * 2 + hres[0][1].numel() * 4 + hres[0][2].numel() * 4
-        e2e = {"value": round(job_flops / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-               "ms_per_step": round(ms_e2e, 3), "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
-               "overlap": "upload of step i+1 and download of step i-1 on copy streams during the "
-                          "forward of step i (two buffer sets); first upload and last download timed",
-               "serial_ms_per_step": round(ms_serial, 3),
-               "serial_value": round(job_flops / (ms_serial * 1e-3) / 1e12, 2)}
-        bsa.check(bsa.get_device_status(stream), "device status")
-        del dbuf, hres
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
