@@ -86,6 +86,43 @@ __device__ __forceinline__ void decode_item(const DecParams &p, const int32_t *i
   it.j1 = min(nk, it.j0 + p.split);
 }
 
+// Run by one warp before the kernel waits for the previous kernel on the
+// stream: the K tiles of work item blockIdx.x, the item this CTA most likely
+// claims first, for L2, while the previous kernel's last CTAs finish. The
+// lengths are read before they are guaranteed to be final, so a stale value
+// only misplaces a prefetch (the TMA bounds its coordinates; the real tables
+// are computed after the wait). Batches of at most 32 sequences.
+__device__ __forceinline__ void prefetch_first_item(const DecParams &p, const CUtensorMap *tk,
+                                                    int lane) {
+  if (p.n_seqs > 32) return;
+  int ni = 0, ak = 0, nk = 0;   // lane s: sequence s's items, first key, key tiles
+  if (lane < p.n_seqs) {
+    const int q0 = __ldcv(p.cu_q + lane), q1 = __ldcv(p.cu_q + lane + 1);
+    ak = __ldcv(p.cu_k + lane);
+    const int lk = __ldcv(p.cu_k + lane + 1) - ak;
+    if (q1 > q0 && lk > 0) {
+      nk = (lk + kTile - 1) / kTile;
+      ni = p.Hkv * ((nk + p.split - 1) / p.split);
+    }
+  }
+  int incl = ni;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  const int b = blockIdx.x;
+  if (ni > 0 && incl - ni <= b && b < incl) {   // at most one lane: the item's sequence
+    const int local = b - (incl - ni);
+    const int q = local / p.Hkv, kvh = local - q * p.Hkv;
+    const int j0 = q * p.split, j1 = min(nk, j0 + p.split);
+    for (int j = j0; j < j1; ++j) {
+      tma_prefetch_3d(tk, 0, kvh, ak + j * kTile);
+      tma_prefetch_3d(tk, 64, kvh, ak + j * kTile);
+    }
+  }
+}
+
 // One 128-key tile of K or V (both 64-column boxes); K and V are read once,
 // so their lines leave L2 first and the per-item tables stay.
 __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, uint64_t *bar,
@@ -421,6 +458,7 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_sh;
+  if (warp == 8) prefetch_first_item(p, &tk, lane);
   grid_dep_wait();     // the previous kernel on the stream is done
   grid_dep_launch();
   const uint64_t limit = p.wait_limit_ns;
