@@ -21,8 +21,8 @@
 //    most 64 rows and an even group, an item takes two query heads of the
 //    group instead: the last 64 positions of each fill the tile's two halves,
 //    so every MMA row and every epilogue lane carries a window row. S = Q K^T goes to one
-//    of two TMEM buffers (128 columns each) while the epilogue reduces the
-//    other: per row, t = max(S c) and e = sum exp2(S c - t) over the keys the
+//    of four TMEM buffers (128 columns each), so the MMAs run up to three
+//    tiles ahead of the epilogue reducing the oldest: per row, t = max(S c) and e = sum exp2(S c - t) over the keys the
 //    row may see, written to a [head][block][row] table.
 //      warp 0 lane 0   TMA producer (Q double buffer, 4-stage K ring)
 //      warp 1          TMEM allocation; lane 0 issues tcgen05.mma
@@ -51,6 +51,7 @@ namespace {
 constexpr uint32_t kTileBytes = 32768;   // 128 rows x 128 bf16
 constexpr uint32_t kBoxBytes = 16384;    // one 128-row x 128-byte TMA box
 constexpr int kKStages = 4;
+constexpr int kSBufs = 4;   // S buffers in TMEM (128 columns each): the MMA runs 3 tiles ahead
 constexpr uint32_t SM_Q = 0, SM_K = 2 * kTileBytes, SM_BYTES = SM_K + kKStages * kTileBytes;
 constexpr uint32_t kIdesc = IDesc<1, false, 128, 128>::value;   // bf16 x bf16 -> f32, M = N = 128
 
@@ -60,8 +61,8 @@ enum : int {
   I_KF = I_QE + 2,          // K ring
   I_KE = I_KF + kKStages,
   I_SF = I_KE + kKStages,   // S buffer written by the MMA
-  I_SE = I_SF + 2,          // S buffer read by the four epilogue warps
-  I_DRAIN = I_SE + 2,
+  I_SE = I_SF + kSBufs,     // S buffer read by the four epilogue warps
+  I_DRAIN = I_SE + kSBufs,
   I_COUNT
 };
 
@@ -157,12 +158,12 @@ __global__ void __launch_bounds__(kImpThreads, 1) imp_tiles_kernel(const __grid_
   const uint64_t limit = p.wait_limit_ns;
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < I_COUNT; ++b) mbar_init(&bar[b], (b == I_SE || b == I_SE + 1) ? 4 : 1);
+    for (int b = 0; b < I_COUNT; ++b) mbar_init(&bar[b], (b >= I_SE && b < I_SE + kSBufs) ? 4 : 1);
     fence_mbar_init();
     abort_sh = 0;
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_sh, 256);
+    tmem_alloc(&tmem_sh, 128 * kSBufs);
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -179,7 +180,8 @@ __global__ void __launch_bounds__(kImpThreads, 1) imp_tiles_kernel(const __grid_
       // ------------------------------------------------ TMA producer
       const void *tq = &p.iw->tmap[0], *tk = &p.iw->tmap[1];
       uint32_t qi = 0, kc = 0;
-      int q_last[2] = {-1, -1}, k_last[kKStages] = {-1, -1, -1, -1};
+      int q_last[2] = {-1, -1}, k_last[kKStages];
+      for (int st = 0; st < kKStages; ++st) k_last[st] = -1;
       for (int item = blockIdx.x; item < total && !abort_sh; item += gridDim.x) {
         Item it;
         decode_item(p, item, it);
@@ -240,9 +242,9 @@ __global__ void __launch_bounds__(kImpThreads, 1) imp_tiles_kernel(const __grid_
         tc_fence_after();
         const uint32_t qs = sbase + SM_Q + qb * kTileBytes;
         for (int g = it.g0; g < it.g1; ++g) {
-          const uint32_t st = kc % kKStages, sb = sc & 1;
+          const uint32_t st = kc % kKStages, sb = sc % kSBufs;
           if (!(ok = mbar_wait(&bar[I_KF + st], (kc / kKStages) & 1, limit))) break;
-          if (!(ok = mbar_wait(&bar[I_SE + sb], ((sc >> 1) & 1) ^ 1, limit))) break;
+          if (!(ok = mbar_wait(&bar[I_SE + sb], ((sc / kSBufs) & 1) ^ 1, limit))) break;
           tc_fence_after();
           const uint32_t ks = sbase + SM_K + st * kTileBytes;
           // K-major A and B, 128-byte swizzle: a K step of 16 is 32 bytes
@@ -288,9 +290,9 @@ __global__ void __launch_bounds__(kImpThreads, 1) imp_tiles_kernel(const __grid_
       float *te = p.stat_e + ((int64_t)hh * p.total_blocks + p.blk_off[it.s]) * kTile + wrow;
       float cm = -INFINITY, cl = 0.f;   // (t, e) combined over this chunk
       for (int g = it.g0; g < it.g1; ++g) {
-        const uint32_t sb = sc & 1;
+        const uint32_t sb = sc % kSBufs;
         // warp-uniform outcome: the TMEM loads below are warp-collective
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar[I_SF + sb], (sc >> 1) & 1, limit));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar[I_SF + sb], (sc / kSBufs) & 1, limit));
         if (!ok) break;
         tc_fence_after();
         uint32_t v[4][32];
@@ -356,7 +358,7 @@ __global__ void __launch_bounds__(kImpThreads, 1) imp_tiles_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   if (abort_sh && threadIdx.x == 0) atomicOr(&p.ws->status, kStatusTimeout);
-  if (warp == 1) tmem_dealloc(tmem, 256);
+  if (warp == 1) tmem_dealloc(tmem, 128 * kSBufs);
 }
 
 // ============================================================ reductions
