@@ -167,6 +167,11 @@ __device__ __forceinline__ uint32_t counter_add_acq_rel(uint64_t *a) {
   asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], 1;" : "=l"(old) : "l"(a) : "memory");
   return (uint32_t)old;
 }
+__device__ __forceinline__ uint32_t counter_add_acquire(uint64_t *a) {
+  uint64_t old;
+  asm volatile("atom.acquire.gpu.global.add.u64 %0, [%1], 1;" : "=l"(old) : "l"(a) : "memory");
+  return (uint32_t)old;
+}
 
 // Wait for a phase of an mbarrier; false when the CTA is aborting or the wait
 // ran past the limit (then the CTA aborts).
@@ -1001,13 +1006,17 @@ dec_kernel(const __grid_constant__ DecParams p, const __grid_constant__ CUtensor
       // 0's count by the barrier, and the count (acq_rel, gpu scope) releases
       // them with it: the CTA whose count completes the (sequence, KV head)
       // acquires every earlier count's writes, and its barrier hands them to
-      // its whole group, which reads them from L2.
+      // its whole group, which reads them from L2. A split without a partial
+      // result counts with acquire only: it has nothing to release, and its
+      // read-modify-write still continues the release sequences of the
+      // counts before it.
       named_bar_sync(2, kGroup);
       if (tp == 0) {   // the last of the splits of this (sequence, KV head) merges
         if (n > 0) p.flags[item] = p.epoch;
         uint64_t *done = p.done + it.s * p.Hkv + it.kvh;
         counter_enter(done, p.epoch);
-        merge_sh = counter_add_acq_rel(done) == (uint32_t)(it.ns - 1);
+        const uint32_t before = n > 0 ? counter_add_acq_rel(done) : counter_add_acquire(done);
+        merge_sh = before == (uint32_t)(it.ns - 1);
       }
       named_bar_sync(2, kGroup);
       if (!merge_sh) continue;
