@@ -329,13 +329,25 @@ __global__ void __launch_bounds__(kImpThreads, 1) imp_tiles_kernel(const __grid_
         float t = -INFINITY, sum = 0.f;
         if (mx > -INFINITY) {
           t = mx * p.c;
-          float s4[4] = {0.f, 0.f, 0.f, 0.f};
+          // two columns per instruction: packed f32x2 scale-and-subtract and
+          // sums (eight partial sums), the exponentials one by one
+          const uint64_t c2 = f2_pack(p.c, p.c), nt2 = f2_pack(-t, -t);
+          uint64_t s2[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) s2[k] = f2_pack(0.f, 0.f);
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              s4[e & 3] += ex2_approx(fmaf(__uint_as_float(v[ch][e]), p.c, -t));
-          sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+            for (int e = 0; e < 32; e += 2) {
+              float y0, y1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(v[ch][e]), __uint_as_float(v[ch][e + 1])), c2, nt2),
+                        y0, y1);
+              s2[(e >> 1) & 3] = f2_add(s2[(e >> 1) & 3], f2_pack(ex2_approx(y0), ex2_approx(y1)));
+            }
+          float s8[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) f2_unpack(s2[k], s8[2 * k], s8[2 * k + 1]);
+          sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
         }
         tt[(int64_t)g * kTile] = t;
         te[(int64_t)g * kTile] = sum;
