@@ -20,10 +20,14 @@
 //    window are ignored); each key block is one K tile. For a window of at
 //    most 64 rows and an even group, an item takes two query heads of the
 //    group instead: the last 64 positions of each fill the tile's two halves,
-//    so every MMA row and every epilogue lane carries a window row. S = Q K^T goes to one
-//    of four TMEM buffers (128 columns each), so the MMAs run up to three
-//    tiles ahead of the epilogue reducing the oldest: per row, t = max(S c) and e = sum exp2(S c - t) over the keys the
-//    row may see, written to a [head][block][row] table.
+//    so every MMA row and every epilogue lane carries a window row.
+//    S = Q K^T goes to one of four TMEM buffers (128 columns each), so the
+//    MMAs run up to three tiles ahead of the epilogue reducing the oldest:
+//    per row, a reference t and e = sum exp2(S c - t) over the keys the row
+//    may see, written to a [head][block][row] table. t is the running max
+//    of the chunk's earlier tiles (e 2^t does not depend on t), or the
+//    tile's own max for a chunk's first tile and for a tile whose sum would
+//    overflow against the running max.
 //      warp 0 lane 0   TMA producer (Q double buffer, 4-stage K ring)
 //      warp 1          TMEM allocation; lane 0 issues tcgen05.mma
 //      warps 2-5       epilogue, TMEM lane quarter = warp % 4
@@ -318,20 +322,14 @@ __global__ void __launch_bounds__(kImpThreads, 1) imp_tiles_kernel(const __grid_
             for (int e = 0; e < 32; ++e)
               if (ch * 32 + e >= ncol) v[ch][e] = __float_as_uint(-INFINITY);
         }
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            m4[(e >> 1) & 3] = max3f(m4[(e >> 1) & 3], __uint_as_float(v[ch][e]),
-                                     __uint_as_float(v[ch][e + 1]));
-        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        float t = -INFINITY, sum = 0.f;
-        if (mx > -INFINITY) {
-          t = mx * p.c;
+        // (t, e) of the tile against a reference t: the chunk's running max
+        // once it has one (any reference gives the same e 2^t; a tile more
+        // than 2^127 above it overflows and is redone against its own max),
+        // else the tile's own max
+        auto exp_sum = [&](float tref) -> float {
           // two columns per instruction: packed f32x2 scale-and-subtract and
           // sums (eight partial sums), the exponentials one by one
-          const uint64_t c2 = f2_pack(p.c, p.c), nt2 = f2_pack(-t, -t);
+          const uint64_t c2 = f2_pack(p.c, p.c), nt2 = f2_pack(-tref, -tref);
           uint64_t s2[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) s2[k] = f2_pack(0.f, 0.f);
@@ -347,7 +345,30 @@ __global__ void __launch_bounds__(kImpThreads, 1) imp_tiles_kernel(const __grid_
           float s8[8];
 #pragma unroll
           for (int k = 0; k < 4; ++k) f2_unpack(s2[k], s8[2 * k], s8[2 * k + 1]);
-          sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+          return ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+        };
+        float t = -INFINITY, sum = 0.f;
+        bool own = !(cm > -INFINITY);
+        if (!own) {
+          t = cm;
+          sum = exp_sum(t);
+          own = !(sum < INFINITY);
+        }
+        if (own) {
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+            for (int e = 0; e < 32; e += 2)
+              m4[(e >> 1) & 3] = max3f(m4[(e >> 1) & 3], __uint_as_float(v[ch][e]),
+                                       __uint_as_float(v[ch][e + 1]));
+          const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          t = -INFINITY;
+          sum = 0.f;
+          if (mx > -INFINITY) {
+            t = mx * p.c;
+            sum = exp_sum(t);
+          }
         }
         tt[(int64_t)g * kTile] = t;
         te[(int64_t)g * kTile] = sum;

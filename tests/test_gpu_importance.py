@@ -129,6 +129,28 @@ def test_empty_sequence_and_window_longer_than_sequence():
     check_scores(sc.cpu().numpy(), want)
 
 
+def test_block_far_above_the_earlier_blocks_of_its_chunk():
+    """A key block whose scores exceed every earlier block of its 16-block
+    chunk by far more than 127 in log2 units (its keys scaled by 256): the
+    kernel takes a tile's (t, e) against the chunk's running maximum, so this
+    tile's sum overflows and is taken again against the tile's own maximum.
+    Block scores and head means against the oracle, causal and not."""
+    base = gi.small("imp_far", [700], Hq=4, Hkv=1, seed=11)
+    k = gi.bf16_bits_to_f32(base.k)
+    k[3 * G:4 * G] *= 256.0
+    p = gi.Problem("imp_far", base.q, gi.bf16_bits_from_f32(k), base.v, base.cu_seqlens, 4, 1, 128)
+    qf, kf = gi.bf16_bits_to_f32(p.q), gi.bf16_bits_to_f32(p.k)
+    s3 = np.einsum("hd,kd->hk", qf[-1], kf[3 * G:4 * G, 0]) / np.sqrt(128.0) * np.log2(np.e)
+    s0 = np.einsum("hd,kd->hk", qf[-1], kf[:3 * G, 0]) / np.sqrt(128.0) * np.log2(np.e)
+    assert (s3.max(axis=1) - s0.max(axis=1)).max() > 200   # the case is what it claims
+    for n, causal in ((64, True), (128, False)):
+        sc, mn, st = run_importance(p, n, causal)
+        assert st == 0
+        want = imp.block_importance(p.q, p.k, p.cu_seqlens, 4, 1, n, causal)
+        print(n, causal, "max rel err", check_scores(sc.cpu().numpy(), want))
+        check_scores(mn.cpu().numpy(), imp.head_mean(want))
+
+
 def test_full_size_mass_and_sampled_heads():
     """The 128K Llama-shaped layer: every head's scores add up to 1/128, and
     four heads (one per KV group pair) match the oracle."""
